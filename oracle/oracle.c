@@ -1,0 +1,408 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for context-parallel attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no source,
+ * header, table or helper with the CUDA library in context_attention_gb300/,
+ * and the CUDA library never calls it.
+ *
+ * Every value is computed in double precision from the stored input values
+ * (fp32 arrays; bf16 inputs are passed already widened, which is exact).
+ * Nothing here is blocked, fused or reordered beyond what the definitions
+ * below state: each function is the definition written out.
+ *
+ * Sources (pages on context parallelism):
+ *  - "Kernel reference: ring_attention_const_max_fwd", sections "Overview"
+ *    (ring schedule, step t on rank r uses the K/V of rank r-t), "Picking a
+ *    max that is safe without measuring it" (c_i = scale*|q_i|*max_j|k_j|),
+ *    "A static bound makes the ring reduction pure addition" and "Accumulate,
+ *    then normalize once" (unnormalised sums, clamp 1e-37, lse = c + log sum).
+ *  - "DCP (Decode Context Parallelism)", sections "Decode Compute Pattern"
+ *    (partial attention + LSE, weight_i = exp(local_lse - global_lse)),
+ *    "local_filled Computation", "Active Token Handling and dcp_active_mask",
+ *    "Slot Mapping and KV Cache" (block b of I tokens lives on rank b mod W)
+ *    and "Segmented Attention CP" (local slot s -> global (s//I)*(W*I)+R*I+s%I).
+ *  - "Sharding the Input" (striped layout: token t on device t mod cp;
+ *    causal masking: a later token never influences an earlier one).
+ *
+ * Parity pins: every function here is pinned by the not-gpu tests in
+ * tests/test_oracle_pins.py and tests/test_index_maps.py (closed forms,
+ * invariants, brute force on tiny inputs, the pages' worked examples).
+ * No function is left "parity unpinned".
+ *
+ * Row conventions.  q is [B, Hq, S, D], k and v are [B, Hkv, S, D], all
+ * row-major.  The S rows of a head are stored shard-major: row rho = r*Ls + a
+ * is local token a of virtual shard r (Ls = S / cp).  Its global token
+ * position is rho for the contiguous layout and a*cp + r for the striped one.
+ * Query head h reads key/value head h / (Hq/Hkv).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORA_LAYOUT_CONTIGUOUS 0
+#define ORA_LAYOUT_STRIPED 1
+
+/* Global token position of stored row rho (see the row conventions above).
+ * Contiguous: shard r holds tokens [r*Ls, (r+1)*Ls) in order.
+ * Striped: token t is dealt to shard t mod cp as its (t div cp)-th token. */
+static int64_t global_pos(int layout, int cp, int64_t Ls, int64_t rho) {
+  int64_t r = rho / Ls, a = rho % Ls;
+  if (layout == ORA_LAYOUT_STRIPED) return a * cp + r;
+  return r * Ls + a;
+}
+
+int64_t ora_global_pos(int layout, int cp, int64_t Ls, int64_t rho) {
+  return global_pos(layout, cp, Ls, rho);
+}
+
+/* One query row against the keys with stored index in [k_begin, k_end) that
+ * the causal rule allows.  Writes the normalised output and the natural-log
+ * LSE (scale included).  Empty allowed set: o = 0, lse = -inf. */
+static void attend_row(const float *qrow, const float *kh, const float *vh,
+                       int64_t S, int D, double scale, int causal, int layout,
+                       int cp, int64_t qrho, int64_t k_begin, int64_t k_end,
+                       double *orow, double *lse_out) {
+  int64_t Ls = S / cp;
+  int64_t qpos = global_pos(layout, cp, Ls, qrho);
+  double *s = (double *)malloc(sizeof(double) * (size_t)(k_end - k_begin + 1));
+  double m = -INFINITY;
+  for (int64_t j = k_begin; j < k_end; ++j) {
+    int allowed = 1;
+    if (causal) allowed = global_pos(layout, cp, Ls, j) <= qpos;
+    if (!allowed) {
+      s[j - k_begin] = -INFINITY;
+      continue;
+    }
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d) dot += (double)qrow[d] * (double)kh[j * D + d];
+    s[j - k_begin] = scale * dot;
+    if (s[j - k_begin] > m) m = s[j - k_begin];
+  }
+  for (int d = 0; d < D; ++d) orow[d] = 0.0;
+  if (m == -INFINITY) {
+    *lse_out = -INFINITY;
+    free(s);
+    return;
+  }
+  double l = 0.0;
+  for (int64_t j = k_begin; j < k_end; ++j) {
+    double sj = s[j - k_begin];
+    if (sj == -INFINITY) continue;
+    double p = exp(sj - m);
+    l += p;
+    for (int d = 0; d < D; ++d) orow[d] += p * (double)vh[j * D + d];
+  }
+  for (int d = 0; d < D; ++d) orow[d] /= l;
+  *lse_out = m + log(l);
+  free(s);
+}
+
+/* Full softmax attention for selected rows.  rows[i] is the flat row id
+ * (b*Hq + h)*S + rho.  o is [nrows, D], lse is [nrows]. */
+void ora_attention_rows(const float *q, const float *k, const float *v, int B,
+                        int Hq, int Hkv, int64_t S, int D, double scale,
+                        int causal, int layout, int cp, const int64_t *rows,
+                        int64_t nrows, double *o, double *lse) {
+  int G = Hq / Hkv;
+  (void)B;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t id = rows[i];
+    int64_t rho = id % S;
+    int64_t bh = id / S;
+    int64_t b = bh / Hq, h = bh % Hq;
+    int64_t bk = b * Hkv + h / G;
+    attend_row(q + id * D, k + bk * S * D, v + bk * S * D, S, D, scale, causal,
+               layout, cp, rho, 0, S, o + i * D, lse + i);
+  }
+}
+
+/* Partial attention of selected rows against the keys of one virtual shard
+ * (stored rows [s*Ls, (s+1)*Ls)), with the same causal rule.  This is one ring
+ * step's partial result (o_s normalised over the shard, lse_s). */
+void ora_shard_partial_rows(const float *q, const float *k, const float *v,
+                            int B, int Hq, int Hkv, int64_t S, int D,
+                            double scale, int causal, int layout, int cp,
+                            int kv_shard, const int64_t *rows, int64_t nrows,
+                            double *o, double *lse) {
+  int G = Hq / Hkv;
+  int64_t Ls = S / cp;
+  (void)B;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t id = rows[i];
+    int64_t rho = id % S;
+    int64_t bh = id / S;
+    int64_t b = bh / Hq, h = bh % Hq;
+    int64_t bk = b * Hkv + h / G;
+    attend_row(q + id * D, k + bk * S * D, v + bk * S * D, S, D, scale, causal,
+               layout, cp, rho, (int64_t)kv_shard * Ls,
+               (int64_t)(kv_shard + 1) * Ls, o + i * D, lse + i);
+  }
+}
+
+/* LSE merge of n partials (DCP page, decode steps 5-7):
+ *   M = max_i lse_i (partials with lse = -inf are skipped),
+ *   L = M + ln sum_i exp(lse_i - M),
+ *   o = sum_i exp(lse_i - L) * o_i.
+ * All partials empty: o = 0, L = -inf.
+ * o_parts is [n, nrows, D], lse_parts is [n, nrows]. */
+void ora_lse_merge(const double *o_parts, const double *lse_parts, int n,
+                   int64_t nrows, int D, double *o, double *lse) {
+#pragma omp parallel for
+  for (int64_t r = 0; r < nrows; ++r) {
+    double M = -INFINITY;
+    for (int i = 0; i < n; ++i)
+      if (lse_parts[(int64_t)i * nrows + r] > M) M = lse_parts[(int64_t)i * nrows + r];
+    for (int d = 0; d < D; ++d) o[r * D + d] = 0.0;
+    if (M == -INFINITY) {
+      lse[r] = -INFINITY;
+      continue;
+    }
+    double acc = 0.0;
+    for (int i = 0; i < n; ++i) {
+      double li = lse_parts[(int64_t)i * nrows + r];
+      if (li == -INFINITY) continue;
+      acc += exp(li - M);
+    }
+    double L = M + log(acc);
+    for (int i = 0; i < n; ++i) {
+      double li = lse_parts[(int64_t)i * nrows + r];
+      if (li == -INFINITY) continue;
+      double w = exp(li - L);
+      for (int d = 0; d < D; ++d)
+        o[r * D + d] += w * o_parts[((int64_t)i * nrows + r) * D + d];
+    }
+    lse[r] = L;
+  }
+}
+
+/* Const-max bound (const-max page, "Picking a max ..." and "Assembling the
+ * bound"): kmax2[b, hk] = max over ALL S keys of the head of |k_j|^2, and
+ * c[b, h, rho] = scale * |q_rho| * sqrt(kmax2[b, h / G]).
+ * c is [B, Hq, S], kmax2 is [B, Hkv]. */
+void ora_const_max_bound(const float *q, const float *k, int B, int Hq, int Hkv,
+                         int64_t S, int D, double scale, double *c,
+                         double *kmax2) {
+  int G = Hq / Hkv;
+  for (int64_t bk = 0; bk < (int64_t)B * Hkv; ++bk) {
+    double mx = 0.0;
+    for (int64_t j = 0; j < S; ++j) {
+      double n2 = 0.0;
+      for (int d = 0; d < D; ++d) {
+        double x = (double)k[(bk * S + j) * D + d];
+        n2 += x * x;
+      }
+      if (n2 > mx) mx = n2;
+    }
+    kmax2[bk] = mx;
+  }
+#pragma omp parallel for
+  for (int64_t id = 0; id < (int64_t)B * Hq * S; ++id) {
+    int64_t bh = id / S;
+    int64_t b = bh / Hq, h = bh % Hq;
+    double n2 = 0.0;
+    for (int d = 0; d < D; ++d) {
+      double x = (double)q[id * D + d];
+      n2 += x * x;
+    }
+    c[id] = scale * sqrt(n2) * sqrt(kmax2[b * Hkv + h / G]);
+  }
+}
+
+/* Ring attention for selected rows, step by step as the const-max page's
+ * "Overview" draws it: query row rho lives on shard r = rho / Ls and, at ring
+ * step t = 0..cp-1, meets the keys of shard (r - t) mod cp.
+ *
+ * mode 0 (online max): each step gives a normalised partial (o_t, lse_t) and
+ *   the partials are LSE-merged in ring order (the merge above).
+ * mode 1 (const max): with the bound c (array [B,Hq,S] from
+ *   ora_const_max_bound), every step adds its unnormalised sums
+ *   acc_o += sum_j exp(s_j - c) v_j and acc_l += sum_j exp(s_j - c); at the
+ *   end o = acc_o / max(acc_l, 1e-37) and lse = c + ln(acc_l).
+ *
+ * overshoot (nullable, [nrows]) receives c - max_j s_j in const mode (the
+ * number of nats by which the bound exceeds the row's true maximum); the
+ * page says rows whose overshoot passes ~85 nats underflow in fp32. */
+void ora_ring_rows(const float *q, const float *k, const float *v, int B,
+                   int Hq, int Hkv, int64_t S, int D, double scale, int causal,
+                   int layout, int cp, int mode, const double *c,
+                   const int64_t *rows, int64_t nrows, double *o, double *lse,
+                   double *overshoot) {
+  int G = Hq / Hkv;
+  int64_t Ls = S / cp;
+  (void)B;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < nrows; ++i) {
+    int64_t id = rows[i];
+    int64_t rho = id % S;
+    int64_t bh = id / S;
+    int64_t b = bh / Hq, h = bh % Hq;
+    int64_t bk = b * Hkv + h / G;
+    const float *qrow = q + id * D;
+    const float *kh = k + bk * S * D;
+    const float *vh = v + bk * S * D;
+    int r = (int)(rho / Ls);
+    int64_t qpos = global_pos(layout, cp, Ls, rho);
+    double *orow = o + i * D;
+    if (mode == 0) {
+      double *op = (double *)malloc(sizeof(double) * (size_t)cp * D);
+      double *lp = (double *)malloc(sizeof(double) * (size_t)cp);
+      for (int t = 0; t < cp; ++t) {
+        int s = ((r - t) % cp + cp) % cp;
+        attend_row(qrow, kh, vh, S, D, scale, causal, layout, cp, rho,
+                   (int64_t)s * Ls, (int64_t)(s + 1) * Ls, op + (int64_t)t * D,
+                   lp + t);
+      }
+      /* merge of cp partials for this one row */
+      double M = -INFINITY;
+      for (int t = 0; t < cp; ++t)
+        if (lp[t] > M) M = lp[t];
+      for (int d = 0; d < D; ++d) orow[d] = 0.0;
+      if (M == -INFINITY) {
+        lse[i] = -INFINITY;
+      } else {
+        double acc = 0.0;
+        for (int t = 0; t < cp; ++t)
+          if (lp[t] != -INFINITY) acc += exp(lp[t] - M);
+        double L = M + log(acc);
+        for (int t = 0; t < cp; ++t) {
+          if (lp[t] == -INFINITY) continue;
+          double w = exp(lp[t] - L);
+          for (int d = 0; d < D; ++d) orow[d] += w * op[(int64_t)t * D + d];
+        }
+        lse[i] = L;
+      }
+      if (overshoot) overshoot[i] = NAN;
+      free(op);
+      free(lp);
+    } else {
+      double ci = c[id];
+      double acc_l = 0.0, smax = -INFINITY;
+      for (int d = 0; d < D; ++d) orow[d] = 0.0;
+      for (int t = 0; t < cp; ++t) {
+        int s = ((r - t) % cp + cp) % cp;
+        for (int64_t j = (int64_t)s * Ls; j < (int64_t)(s + 1) * Ls; ++j) {
+          if (causal && global_pos(layout, cp, Ls, j) > qpos) continue;
+          double dot = 0.0;
+          for (int d = 0; d < D; ++d) dot += (double)qrow[d] * (double)kh[j * D + d];
+          double sj = scale * dot;
+          if (sj > smax) smax = sj;
+          double p = exp(sj - ci);
+          acc_l += p;
+          for (int d = 0; d < D; ++d) orow[d] += p * (double)vh[j * D + d];
+        }
+      }
+      double denom = acc_l > 1e-37 ? acc_l : 1e-37;
+      for (int d = 0; d < D; ++d) orow[d] /= denom;
+      lse[i] = ci + log(acc_l);
+      if (overshoot) overshoot[i] = ci - smax;
+    }
+  }
+}
+
+/* ---------------------------------------------------------------------------
+ * DCP index maps, by enumeration.  The DCP page's "Slot Mapping and KV Cache"
+ * deals blocks of I consecutive tokens to the W ranks round robin (block 0 to
+ * rank 0, block 1 to rank 1, ..., block W to rank 0 again).  The functions
+ * below simulate that dealing token by token; they never evaluate the closed
+ * forms that the CUDA library uses.
+ * ------------------------------------------------------------------------- */
+
+/* For global positions 0..n-1: owner rank and local index on that rank. */
+void ora_dcp_deal(int64_t n, int W, int I, int32_t *owner, int64_t *local) {
+  int rank = 0, in_block = 0;
+  int64_t *count = (int64_t *)calloc((size_t)W, sizeof(int64_t));
+  for (int64_t p = 0; p < n; ++p) {
+    owner[p] = rank;
+    local[p] = count[rank]++;
+    if (++in_block == I) {
+      in_block = 0;
+      rank = (rank + 1) % W;
+    }
+  }
+  free(count);
+}
+
+/* Number of tokens among positions 0..N-1 that rank R holds. */
+int64_t ora_dcp_local_filled(int64_t N, int W, int I, int R) {
+  int32_t *own = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
+  int64_t *loc = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
+  ora_dcp_deal(N, W, I, own, loc);
+  int64_t cnt = 0;
+  for (int64_t p = 0; p < N; ++p) cnt += own[p] == R;
+  free(own);
+  free(loc);
+  return cnt;
+}
+
+/* DCP decode for one query token per sequence (DCP page, "Decode Compute
+ * Pattern").  q [N, Hq, D]; k_shards, v_shards [W, N, Hkv, Lloc, D], where
+ * shard r holds its dealt tokens in local order.  Sequence n attends to global
+ * positions [0, seq_lens[n]) (all of them are visible: the decoded token's own
+ * K/V is already in the cache, held by its owner only).  Each rank computes a
+ * partial (o_r, lse_r) over the local slots it holds, then the partials are
+ * LSE-merged.  o [N, Hq, D], lse [N, Hq]. */
+void ora_dcp_decode(const float *q, const float *k_shards,
+                    const float *v_shards, int N, int Hq, int Hkv,
+                    int64_t Lloc, int D, int W, int I, const int64_t *seq_lens,
+                    double scale, double *o, double *lse) {
+  int G = Hq / Hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t nh = 0; nh < (int64_t)N * Hq; ++nh) {
+    int64_t n = nh / Hq, h = nh % Hq, hk = h / G;
+    int64_t L = seq_lens[n];
+    const float *qrow = q + nh * D;
+    /* which local slots of each rank are valid: deal positions 0..L-1 */
+    int32_t *own = (int32_t *)malloc(sizeof(int32_t) * (size_t)(L > 0 ? L : 1));
+    int64_t *loc = (int64_t *)malloc(sizeof(int64_t) * (size_t)(L > 0 ? L : 1));
+    ora_dcp_deal(L, W, I, own, loc);
+    double *op = (double *)calloc((size_t)W * D, sizeof(double));
+    double *lp = (double *)malloc(sizeof(double) * (size_t)W);
+    for (int r = 0; r < W; ++r) {
+      const float *kh = k_shards + (((int64_t)r * N + n) * Hkv + hk) * Lloc * D;
+      const float *vh = v_shards + (((int64_t)r * N + n) * Hkv + hk) * Lloc * D;
+      double m = -INFINITY;
+      for (int64_t p = 0; p < L; ++p) {
+        if (own[p] != r) continue;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += (double)qrow[d] * (double)kh[loc[p] * D + d];
+        if (scale * dot > m) m = scale * dot;
+      }
+      if (m == -INFINITY) {
+        lp[r] = -INFINITY;
+        continue;
+      }
+      double l = 0.0;
+      for (int64_t p = 0; p < L; ++p) {
+        if (own[p] != r) continue;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += (double)qrow[d] * (double)kh[loc[p] * D + d];
+        double w = exp(scale * dot - m);
+        l += w;
+        for (int d = 0; d < D; ++d) op[(int64_t)r * D + d] += w * (double)vh[loc[p] * D + d];
+      }
+      for (int d = 0; d < D; ++d) op[(int64_t)r * D + d] /= l;
+      lp[r] = m + log(l);
+    }
+    ora_lse_merge(op, lp, W, 1, D, o + nh * D, lse + nh);
+    free(own);
+    free(loc);
+    free(op);
+    free(lp);
+  }
+}
+
+/* Number of OpenMP threads a parallel region here would use. */
+int ora_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
