@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the context-parallel attention hot path on GB300.
+
+One JSON line on rank 0.  A step is one pass of the hot path over one batch of
+synthetic input:
+
+* value  -- const-max ring attention prefill on the DiT workload (B=1, H=40,
+  D=128, S=16384, cp=8 contiguous virtual shards, cross-head RMS-normalised
+  q/k, bf16): the bound pass plus the fused ring kernel, inputs resident in
+  HBM.  Unit TFLOP/s of algorithmic work 4*B*H*S^2*D.
+* decode -- DCP decode (64 sequences x 1 token, Hq=32, Hkv=8, D=128, context
+  131072 over dcp=4 shards interleaved in 16-token blocks): split-KV partials
+  plus the LSE merge.  Unit GB/s of K+V bytes read.
+* e2e    -- the prefill step through the public API with pinned host buffers:
+  q, k, v copied host->device and o copied back inside the timed region.
+
+Both workloads' inputs (0.5 GB and 34 GB) are larger than the 129 MB L2, so
+no flush runs between timed iterations.  ``--impl reference`` times the fp64
+CPU oracle (the only reference this method has) on a bounded sample of the
+same workload.  Under torchrun every rank runs an independent replica (the
+method is not sharded across GPUs on this path) and rank 0 reports the
+aggregate over ranks with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ring-attn prefill TFLOP/s (% bf16 peak); DCP decode KV GB/s (% HBM BW)"
+PREFILL = dict(B=1, H=40, S=16384, D=128, cp=8, seed=2)
+DECODE = dict(N=64, Hq=32, Hkv=8, D=128, W=4, I=16, Lloc=32768, seed=5)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def prefill_flops(c=PREFILL):
+    return 4.0 * c["B"] * c["H"] * c["S"] ** 2 * c["D"]
+
+
+def decode_bytes(c=DECODE):
+    return 2.0 * c["W"] * c["N"] * c["Hkv"] * c["Lloc"] * c["D"] * 2
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def read_traffic(name):
+    """Per-launch DRAM bytes recorded from an ncu capture (profiles/*.txt)."""
+    p = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        for line in f:
+            if line.startswith("traffic_bytes_per_launch:"):
+                v = line.split(":", 1)[1].strip()
+                return None if v in ("", "null") else float(v)
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxs.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs), "samples": len(sms),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup(n_gpus):
+    import torch
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus and world > 1:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}")
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        pg = dist
+    return rank, world, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(x, pg):
+    if pg is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- ours
+
+
+def bench_prefill(ca, torch, steps, warmup, pg, dev_index):
+    from context_attention_gb300 import synth
+
+    c = PREFILL
+    q, k, v = synth.dit_qk(c["B"], c["H"], c["S"], c["D"], seed=c["seed"], device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(c["B"], c["H"], c["S"], device="cuda", dtype=torch.float32)
+    cbound = torch.empty(c["B"], c["H"], c["S"], device="cuda", dtype=torch.float32)
+    kmax2 = torch.empty(c["B"], c["H"], device="cuda", dtype=torch.float32)
+    lib = ca._load()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        st = lib.ca_const_max_bound(q.data_ptr(), k.data_ptr(), 1, c["B"], c["H"], c["H"], c["S"], c["D"], 0.0,
+                                    cbound.data_ptr(), kmax2.data_ptr(), stream.cuda_stream)
+        assert st == 0, st
+        ev_mid = torch.cuda.Event(enable_timing=True)
+        ev_mid.record(stream)
+        st = lib.ca_ring_attn_fwd_bounded(q.data_ptr(), k.data_ptr(), v.data_ptr(), cbound.data_ptr(),
+                                          o.data_ptr(), lse.data_ptr(), 1, c["B"], c["H"], c["H"], c["S"], c["D"],
+                                          c["cp"], 0, 0, 0.0, stream.cuda_stream)
+        assert st == 0, st
+        return ev_mid
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(pg)
+    torch.cuda.synchronize()
+    evs = []
+    with ClockSampler(dev_index) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        prev = t_start
+        for _ in range(steps):
+            mid = step()
+            end = torch.cuda.Event(enable_timing=True)
+            end.record(stream)
+            evs.append((prev, mid, end))
+            prev = end
+        torch.cuda.synchronize()
+    barrier(pg)
+    torch.cuda.synchronize()
+    total_ms = t_start.elapsed_time(prev)
+    ring_ms = [m.elapsed_time(e) for _, m, e in evs]
+    bound_ms = [s.elapsed_time(m) for s, m, _ in evs]
+    assert ca.device_status() == 0
+    res = dict(total_ms=total_ms, ring_ms=statistics.mean(ring_ms), bound_ms=statistics.mean(bound_ms),
+               clocks=clk.summary())
+    # e2e: through the public API from pinned host memory, copies inside
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(ca.ring_attn_fwd_workspace_size(c["B"], c["H"], c["H"], c["S"], c["D"], c["cp"], "const_max"),
+                     dtype=torch.uint8, device="cuda")
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        out, _ = ca.ring_attn_fwd(qd, kd, vd, c["cp"], mode="const_max", out=o, lse=lse, workspace=ws)
+        oh.copy_(out, non_blocking=True)
+
+    e2e_steps = max(2, min(steps, 5))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    res["e2e_ms"] = a.elapsed_time(b) / e2e_steps
+    res["h2d_bytes"] = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    res["d2h_bytes"] = oh.numel() * oh.element_size()
+    del q, k, v, o, qd, kd, vd, qh, kh, vh, oh
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_decode(ca, torch, steps, warmup, pg):
+    from context_attention_gb300 import synth
+
+    c = DECODE
+    q, k, v = synth.decode_inputs(c["N"], c["Hq"], c["Hkv"], c["D"], c["W"], c["Lloc"], c["seed"], device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(c["N"], c["Hq"], device="cuda", dtype=torch.float32)
+    ws = torch.empty(ca.dcp_decode_workspace_size(c["N"], c["Hq"], c["Hkv"], c["Lloc"], c["D"], c["W"], c["I"]),
+                     dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        ca.dcp_decode(q, k, v, c["I"], out=o, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    barrier(pg)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        ca.dcp_decode(q, k, v, c["I"], out=o, lse=lse, workspace=ws)
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    ms = a.elapsed_time(b) / steps
+    assert ca.device_status() == 0
+    del q, k, v
+    torch.cuda.empty_cache()
+    return dict(ms=ms)
+
+
+def cpu_baseline_prefill(torch, seconds=15.0):
+    """The oracle as it stands, on a bounded sample of DiT-workload rows."""
+    import numpy as np
+
+    import oracle
+    from context_attention_gb300 import synth
+
+    c = PREFILL
+    # one head of the same workload, generated on the host
+    q, k, v = synth.dit_qk(1, c["H"], c["S"], c["D"], seed=c["seed"], device="cpu")
+    qq, kk, vv = (t[:, :1].float().numpy() for t in (q, k, v))
+    bound, _ = oracle.const_max_bound(qq, kk)
+    rng = np.random.default_rng(0)
+
+    def run(n):
+        rows = np.sort(rng.choice(c["S"], size=n, replace=False))
+        t0 = time.perf_counter()
+        oracle.ring(qq, kk, vv, c["cp"], mode=oracle.MODE_CONST_MAX, rows=rows, c=bound)
+        return time.perf_counter() - t0
+
+    t_probe = run(64)
+    n = int(min(c["S"], max(64, 64 * seconds / max(t_probe, 1e-6))))
+    t = run(n)
+    flops = 4.0 * c["S"] * c["D"] * n
+    return dict(value=flops / t / 1e12, unit="TFLOP/s", cores=oracle.num_threads(),
+                kind="oracle", sample=f"{n} query rows of head 0 of the DiT workload (const max), {t:.1f} s",
+                seconds=t)
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    import context_attention_gb300 as ca
+
+    ca._load()
+    peaks, peak_src = load_peaks()
+    pre = bench_prefill(ca, torch, args.steps, args.warmup, pg, local)
+    dec = None if args.skip_decode else bench_decode(ca, torch, args.steps, args.warmup, pg)
+
+    total_ms = max_over_ranks(pre["total_ms"], pg)
+    ms_per_step = total_ms / args.steps
+    flops = prefill_flops()
+    value = world * flops * args.steps / (total_ms / 1e3) / 1e12
+    long_run = total_ms > 2000.0
+    peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
+    ring_tflops = flops / (pre["ring_ms"] / 1e3) / 1e12
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; cross-head RMS-normalised q/k, N(0,1) v)",
+        "config": {"workload": "DiT const-max ring self-attention prefill", "B": PREFILL["B"], "H": PREFILL["H"],
+                   "S": PREFILL["S"], "D": PREFILL["D"], "cp_size": PREFILL["cp"], "mode": "const_max",
+                   "layout": "contiguous", "causal": False, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "pct_of_bf16_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {"kernel": "ring_tc_kernel", "bound": "tensor", "achieved": round(ring_tflops, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(ring_tflops / peak, 4),
+                     "traffic": read_traffic("ring_tc_kernel_dit16k.txt"),
+                     "peak_source": f"{peak_src} {'sustained' if long_run else 'burst'} bf16",
+                     "bound_pass_ms": round(pre["bound_ms"], 4), "ring_ms": round(pre["ring_ms"], 4)},
+        "clocks": pre["clocks"],
+        "e2e": {"value": round(flops / (pre["e2e_ms"] / 1e3) / 1e12 * world, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": pre["h2d_bytes"], "d2h_bytes_per_step": pre["d2h_bytes"],
+                "ms_per_step": round(pre["e2e_ms"], 3)},
+        "gpu_launches": 3 * args.steps + (2 * args.steps if dec else 0),
+    }
+    if dec:
+        dms = max_over_ranks(dec["ms"], pg)
+        gbs = decode_bytes() / (dms / 1e3) / 1e9
+        out["decode"] = {"workload": "DCP decode: 64 seqs x 1 token, Hq=32, Hkv=8, D=128, L=131072, dcp=4, I=16",
+                         "value": round(gbs * world, 1), "unit": "GB/s", "ms_per_step": round(dms, 4),
+                         "pct_of_hbm": round(100.0 * gbs / peaks["hbm_gbs"], 2),
+                         "roofline": {"kernel": "dcp_decode_kernel + lse_merge_kernel", "bound": "hbm",
+                                      "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                      "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                      "traffic": read_traffic("dcp_decode_kernel_131k.txt"),
+                                      "peak_source": f"{peak_src} copy bandwidth"}}
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_prefill(torch, seconds=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- reference arm
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+
+    import oracle
+
+    per_step = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline_prefill(torch, seconds=per_step / 4)
+    vals, secs, samples = [], [], []
+    for _ in range(args.steps):
+        r = cpu_baseline_prefill(torch, seconds=per_step)
+        vals.append(r["value"])
+        secs.append(r["seconds"])
+        samples.append(r["sample"])
+    value = statistics.mean(vals)
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(secs),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded; cross-head RMS-normalised q/k, N(0,1) v)",
+        "config": {"workload": "DiT const-max ring self-attention prefill", "B": PREFILL["B"], "H": PREFILL["H"],
+                   "S": PREFILL["S"], "D": PREFILL["D"], "cp_size": PREFILL["cp"], "mode": "const_max",
+                   "layout": "contiguous", "causal": False, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": samples[-1]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,346 @@
+"""context_attention_gb300 -- GB300-native hot path of context-parallel attention.
+
+A thin ctypes binding over ``libctxattn.so`` (the C ABI in include/ctxattn.h).
+Every function here only checks tensors, allocates outputs and workspaces with
+PyTorch (device memory and streams are PyTorch's job) and passes raw pointers
+plus the current CUDA stream to the library; every step of the computation runs
+in the library's CUDA kernels.  There is no CPU fallback: if the library is
+missing or a call fails, a ``CtxAttnError`` is raised.
+
+Python names mirror the C entry points without the ``ca_`` prefix.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "CtxAttnError", "build", "library_path", "ring_attn_fwd", "ring_attn_fwd_bounded", "attn_partial_step", "lse_merge",
+    "const_max_bound", "dcp_decode", "layout_to_shards", "layout_from_shards", "dcp_shard_kv",
+    "layout_global_index", "layout_shard_row", "ring_kv_shard", "dcp_owner", "dcp_local_index",
+    "dcp_local_to_global", "dcp_local_filled", "dcp_active_mask", "dcp_slot_mapping",
+    "device_status", "ring_attn_fwd_workspace_size", "dcp_decode_workspace_size",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libctxattn.so")
+_lock = threading.Lock()
+_lib = None
+
+CA_OK = 0
+STATUS = {0: "CA_OK", 1: "CA_ERR_INVALID_ARG", 2: "CA_ERR_SHAPE", 3: "CA_ERR_UNSUPPORTED",
+          4: "CA_ERR_ALIGNMENT", 5: "CA_ERR_WORKSPACE", 6: "CA_ERR_CUDA", 7: "CA_ERR_TIMEOUT"}
+DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+MODE = {"online_max": 0, "const_max": 1}
+LAYOUT = {"contiguous": 0, "striped": 1}
+
+
+class CtxAttnError(RuntimeError):
+    """A libctxattn call returned an error status."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libctxattn.so in-tree for sm_103a (see _build.py)."""
+    from . import _build
+
+    return _build.build(force=force, verbose=verbose)
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise CtxAttnError("load libctxattn.so (not built: run context_attention_gb300.build())", 6)
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, I64, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        sig = {
+            "ca_status_string": ([I], ctypes.c_char_p),
+            "ca_version": ([], I),
+            "ca_ring_attn_fwd_workspace_size": ([I, I, I, I64, I, I, I], SZ),
+            "ca_ring_attn_fwd": ([P, P, P, P, P, I, I, I, I, I64, I, I, I, I, I, F, P, SZ, P], I),
+            "ca_ring_attn_fwd_bounded": ([P, P, P, P, P, P, I, I, I, I, I64, I, I, I, I, F, P], I),
+            "ca_attn_partial_step": ([P, P, P, I, I, I, I, I64, I, I, I, I, I, I, I, F, P, P, P, P], I),
+            "ca_lse_merge": ([P, P, I, I64, I, P, P, I, P, P], I),
+            "ca_const_max_bound": ([P, P, I, I, I, I, I64, I, F, P, P, P], I),
+            "ca_dcp_decode_workspace_size": ([I, I, I, I64, I, I, I], SZ),
+            "ca_dcp_decode": ([P, P, P, I, I, I, I, I64, I, I, I, P, F, P, P, P, SZ, P], I),
+            "ca_layout_to_shards": ([P, P, I64, I64, I64, I, I, P], I),
+            "ca_layout_from_shards": ([P, P, I64, I64, I64, I, I, P], I),
+            "ca_dcp_shard_kv": ([P, P, I64, I64, I64, I, I, P], I),
+            "ca_layout_global_index": ([I, I, I64, I64], I64),
+            "ca_layout_shard_row": ([I, I, I64, I64], I64),
+            "ca_ring_kv_shard": ([I, I, I], I),
+            "ca_dcp_owner": ([I64, I, I], I),
+            "ca_dcp_local_index": ([I64, I, I], I64),
+            "ca_dcp_local_to_global": ([I64, I, I, I], I64),
+            "ca_dcp_local_filled": ([I64, I, I, I, I], I64),
+            "ca_dcp_active_mask": ([I64, I, I, I, I], I),
+            "ca_dcp_slot_mapping": ([P, I64, P, I64, I, I, I, I, P], I),
+            "ca_device_status": ([I], I),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != CA_OK:
+        raise CtxAttnError(fn, status)
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, ndim: int):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+    if t.dtype not in DTYPE:
+        raise ValueError(f"{name}: dtype {t.dtype} not supported (bf16 or fp32)")
+
+
+def ring_attn_fwd_workspace_size(B, Hq, Hkv, S, D, cp_size, mode="online_max") -> int:
+    return int(_load().ca_ring_attn_fwd_workspace_size(B, Hq, Hkv, S, D, cp_size, MODE[mode]))
+
+
+def ring_attn_fwd(q, k, v, cp_size, mode="online_max", causal=False, layout="contiguous",
+                  softmax_scale=None, out=None, lse=None, return_lse=True, workspace=None):
+    """Ring attention forward over cp_size virtual shards (shard-major rows).
+
+    q [B,Hq,S,D], k/v [B,Hkv,S,D] (bf16 with D=128, or fp32 with D<=128).
+    Returns (o, lse) with o [B,Hq,S,D] in q's dtype and lse [B,Hq,S] fp32."""
+    lib = _load()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, 4)
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty(B, Hq, S, device=q.device, dtype=torch.float32)
+    ws_bytes = int(lib.ca_ring_attn_fwd_workspace_size(B, Hq, Hkv, S, D, cp_size, MODE[mode]))
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, device=q.device, dtype=torch.uint8)
+    st = lib.ca_ring_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse if return_lse else None),
+                              DTYPE[q.dtype], B, Hq, Hkv, S, D, cp_size, MODE[mode], int(bool(causal)),
+                              LAYOUT[layout], float(softmax_scale or 0.0),
+                              _ptr(workspace) if ws_bytes else None,
+                              workspace.numel() if ws_bytes else 0, _stream(q))
+    _check("ca_ring_attn_fwd", st)
+    return out, (lse if return_lse else None)
+
+
+def ring_attn_fwd_bounded(q, k, v, c, cp_size, causal=False, layout="contiguous", softmax_scale=None,
+                          out=None, lse=None, return_lse=True):
+    """Const-max ring attention with a caller-provided bound c [B,Hq,S] fp32."""
+    lib = _load()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, 4)
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty(B, Hq, S, device=q.device, dtype=torch.float32)
+    st = lib.ca_ring_attn_fwd_bounded(_ptr(q), _ptr(k), _ptr(v), _ptr(c.contiguous()), _ptr(out),
+                                      _ptr(lse if return_lse else None), DTYPE[q.dtype], B, Hq, Hkv, S, D,
+                                      cp_size, int(bool(causal)), LAYOUT[layout], float(softmax_scale or 0.0),
+                                      _stream(q))
+    _check("ca_ring_attn_fwd_bounded", st)
+    return out, (lse if return_lse else None)
+
+
+def attn_partial_step(q_shard, k_shard, v_shard, q_rank, kv_rank, cp_size, mode="online_max",
+                      causal=False, layout="contiguous", softmax_scale=None, c=None):
+    """One ring step: queries of shard q_rank against the K/V of shard kv_rank.
+
+    Returns (o_part fp32, lse_part fp32).  In const-max mode pass the shard's
+    rows of the bound c; o_part is then the unnormalised sum."""
+    lib = _load()
+    for n, t in (("q_shard", q_shard), ("k_shard", k_shard), ("v_shard", v_shard)):
+        _need(t, n, 4)
+    B, Hq, Ls, D = q_shard.shape
+    Hkv = k_shard.shape[1]
+    o = torch.empty(B, Hq, Ls, D, device=q_shard.device, dtype=torch.float32)
+    lse = torch.empty(B, Hq, Ls, device=q_shard.device, dtype=torch.float32)
+    if c is not None:
+        c = c.contiguous()
+    st = lib.ca_attn_partial_step(_ptr(q_shard), _ptr(k_shard), _ptr(v_shard), DTYPE[q_shard.dtype],
+                                  B, Hq, Hkv, Ls, D, q_rank, kv_rank, cp_size, MODE[mode],
+                                  int(bool(causal)), LAYOUT[layout], float(softmax_scale or 0.0),
+                                  _ptr(c), _ptr(o), _ptr(lse), _stream(q_shard))
+    _check("ca_attn_partial_step", st)
+    return o, lse
+
+
+def lse_merge(o_parts, lse_parts, c=None, out_dtype=torch.float32):
+    """Merge n partials o_parts [n, ..., D], lse_parts [n, ...] (fp32)."""
+    lib = _load()
+    if not (o_parts.is_cuda and o_parts.dtype == torch.float32 and o_parts.is_contiguous()):
+        raise ValueError("o_parts must be a contiguous CUDA fp32 tensor")
+    n, D = o_parts.shape[0], o_parts.shape[-1]
+    R = o_parts[0].numel() // D
+    lse_parts = lse_parts.contiguous()
+    o = torch.empty(o_parts.shape[1:], device=o_parts.device, dtype=out_dtype)
+    lse = torch.empty(o_parts.shape[1:-1], device=o_parts.device, dtype=torch.float32)
+    st = lib.ca_lse_merge(_ptr(o_parts), _ptr(lse_parts), n, R, D,
+                          _ptr(c.contiguous()) if c is not None else None, _ptr(o), DTYPE[out_dtype],
+                          _ptr(lse), _stream(o_parts))
+    _check("ca_lse_merge", st)
+    return o, lse
+
+
+def const_max_bound(q, k, softmax_scale=None):
+    """Per-row const-max bound: returns (c [B,Hq,S] fp32, kmax2 [B,Hkv] fp32)."""
+    lib = _load()
+    _need(q, "q", 4)
+    _need(k, "k", 4)
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    c = torch.empty(B, Hq, S, device=q.device, dtype=torch.float32)
+    kmax2 = torch.empty(B, Hkv, device=q.device, dtype=torch.float32)
+    st = lib.ca_const_max_bound(_ptr(q), _ptr(k), DTYPE[q.dtype], B, Hq, Hkv, S, D,
+                                float(softmax_scale or 0.0), _ptr(c), _ptr(kmax2), _stream(q))
+    _check("ca_const_max_bound", st)
+    return c, kmax2
+
+
+def dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, dcp, interleave) -> int:
+    return int(_load().ca_dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, dcp, interleave))
+
+
+def dcp_decode(q, k_shards, v_shards, interleave, seq_lens=None, softmax_scale=None, out=None,
+               lse=None, workspace=None):
+    """DCP decode.  q [N,Hq,D]; k/v shards [dcp,N,Hkv,Lloc,D] (bf16, D=128).
+
+    seq_lens: optional CUDA int32 [N].  Returns (o [N,Hq,D], lse [N,Hq])."""
+    lib = _load()
+    _need(q, "q", 3)
+    _need(k_shards, "k_shards", 5)
+    _need(v_shards, "v_shards", 5)
+    N, Hq, D = q.shape
+    W, _, Hkv, Lloc, _ = k_shards.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(N, Hq, device=q.device, dtype=torch.float32)
+    ws_bytes = int(lib.ca_dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, W, interleave))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), device=q.device, dtype=torch.uint8)
+    if seq_lens is not None:
+        if not (seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()):
+            raise ValueError("seq_lens must be a contiguous CUDA int32 tensor")
+    st = lib.ca_dcp_decode(_ptr(q), _ptr(k_shards), _ptr(v_shards), DTYPE[q.dtype], N, Hq, Hkv, Lloc,
+                           D, W, interleave, _ptr(seq_lens), float(softmax_scale or 0.0), _ptr(out),
+                           _ptr(lse), _ptr(workspace), workspace.numel(), _stream(q))
+    _check("ca_dcp_decode", st)
+    return out, lse
+
+
+def _rows(x: torch.Tensor):
+    if not (x.is_cuda and x.is_contiguous() and x.dim() >= 3):
+        raise ValueError("expected a contiguous CUDA tensor [..., S, D]")
+    S = x.shape[-2]
+    BH = x.numel() // (S * x.shape[-1])
+    return BH, S, x.shape[-1] * x.element_size()
+
+
+def layout_to_shards(x, cp_size, layout="contiguous"):
+    """Rows of x [..., S, D] from global token order into shard-major order."""
+    BH, S, rb = _rows(x)
+    y = torch.empty_like(x)
+    _check("ca_layout_to_shards", _load().ca_layout_to_shards(_ptr(x), _ptr(y), BH, S, rb, cp_size,
+                                                               LAYOUT[layout], _stream(x)))
+    return y
+
+
+def layout_from_shards(y, cp_size, layout="contiguous"):
+    """Inverse of layout_to_shards."""
+    BH, S, rb = _rows(y)
+    x = torch.empty_like(y)
+    _check("ca_layout_from_shards", _load().ca_layout_from_shards(_ptr(y), _ptr(x), BH, S, rb, cp_size,
+                                                                   LAYOUT[layout], _stream(y)))
+    return x
+
+
+def dcp_shard_kv(kv, dcp, interleave):
+    """kv [N, Hkv, L, D] in global order -> shards [dcp, N, Hkv, L/dcp, D]."""
+    BH, L, rb = _rows(kv)
+    out = torch.empty((dcp,) + tuple(kv.shape[:-2]) + (L // dcp, kv.shape[-1]), device=kv.device,
+                      dtype=kv.dtype)
+    _check("ca_dcp_shard_kv", _load().ca_dcp_shard_kv(_ptr(kv), _ptr(out), BH, L, rb, dcp, interleave,
+                                                       _stream(kv)))
+    return out
+
+
+# ------------------------------------------------------------- host index helpers
+def layout_global_index(layout, cp_size, Ls, row) -> int:
+    return int(_load().ca_layout_global_index(LAYOUT[layout], cp_size, Ls, row))
+
+
+def layout_shard_row(layout, cp_size, Ls, token) -> int:
+    return int(_load().ca_layout_shard_row(LAYOUT[layout], cp_size, Ls, token))
+
+
+def ring_kv_shard(rank, step, cp_size) -> int:
+    return int(_load().ca_ring_kv_shard(rank, step, cp_size))
+
+
+def dcp_owner(pos, dcp, interleave) -> int:
+    return int(_load().ca_dcp_owner(pos, dcp, interleave))
+
+
+def dcp_local_index(pos, dcp, interleave) -> int:
+    return int(_load().ca_dcp_local_index(pos, dcp, interleave))
+
+
+def dcp_local_to_global(local, rank, dcp, interleave) -> int:
+    return int(_load().ca_dcp_local_to_global(local, rank, dcp, interleave))
+
+
+def dcp_local_filled(N, dcp, interleave, block_size, rank) -> int:
+    return int(_load().ca_dcp_local_filled(N, dcp, interleave, block_size, rank))
+
+
+def dcp_active_mask(N, dcp, interleave, block_size, rank) -> int:
+    return int(_load().ca_dcp_active_mask(N, dcp, interleave, block_size, rank))
+
+
+def dcp_slot_mapping(positions, block_table, block_size, dcp, rank, interleave):
+    """Host slot mapping: -1 for positions `rank` does not own."""
+    import numpy as np
+
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    out = np.zeros(len(pos), dtype=np.int64)
+    st = _load().ca_dcp_slot_mapping(pos.ctypes.data, len(pos), bt.ctypes.data, len(bt), block_size,
+                                      dcp, rank, interleave, out.ctypes.data)
+    _check("ca_dcp_slot_mapping", st)
+    return out
+
+
+def device_status(reset: bool = True) -> int:
+    """Status of the device error word raised by bounded waits (0 = clean)."""
+    return int(_load().ca_device_status(int(reset)))

@@ -1,0 +1,399 @@
+// decode.cu -- split-KV decode over interleaved DCP shards.
+//
+// "DCP (Decode Context Parallelism)", section "Decode Compute Pattern": the
+// gathered query heads of a sequence attend to each rank's local KV shard and
+// produce a partial output plus its log-sum-exp; the partials are combined by
+// the LSE merge (merge.cu).  Section "local_filled Computation" fixes how
+// many local slots of rank r hold tokens of a sequence of length N; every one
+// of them is visible to the decoded token (its own K/V sits on its owner).
+//
+// One GPU holds all dcp shards.  A work item is (rank r, sequence n, KV head,
+// split of the rank's valid slots).  The scan is HBM bound: a TMA producer
+// warp streams 128-token stages (K and V, 64 KB) through a 3-stage ring; four
+// consumer warps each take 32 tokens of a stage.  The G query heads that
+// share a KV head are the N side of warp-level bf16 MMAs (m16n8k16, fp32
+// accumulate): S^T = K Q^T per 16 tokens, then O^T += V^T P^T, with P moved
+// from the accumulator layout to the operand layout by movmatrix.  Row maxima
+// use the same lazy rescale as the prefill kernel (threshold 2^8).  At the end
+// of an item the four warps' partial states are LSE-merged in shared memory
+// and one partial (o, lse) per query head is written.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "index_maps.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace ca {
+namespace {
+
+constexpr int kTok = 128;                      // tokens per stage
+constexpr int kD = 128;
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr uint32_t kBox = kTok * 64 * 2;       // 16 KB: 128 tokens x 64 columns
+constexpr uint32_t kStageBytes = 4 * kBox;     // K halves, V halves
+constexpr int kMaxG = 8;
+
+constexpr uint32_t kSmemStages = 0;
+constexpr uint32_t kSmemMergeO = kStages * kStageBytes;                    // [warps][8][128] f32
+constexpr uint32_t kSmemMergeML = kSmemMergeO + kConsumerWarps * kMaxG * kD * 4;  // [warps][8] m, l
+constexpr uint32_t kSmemBar = kSmemMergeML + kConsumerWarps * kMaxG * 2 * 4;
+constexpr uint32_t kSmemAbort = kSmemBar + (2 * kStages + 1) * 8;
+constexpr uint32_t kSmemUsed = kSmemAbort + 4;
+constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct DecParams {
+  DecodeArgs a;
+  int G;
+  int64_t items;
+  float scale_log2;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+struct Item {
+  int r, n, hkv, split;
+  int64_t t0, ntok;  // first valid local slot of the item, number of tokens
+  int64_t row0;      // first row of the item in the [W*N*Hkv*Lloc, D] view
+};
+
+__device__ __forceinline__ Item item_of(const DecParams& P, int64_t it) {
+  const DecodeArgs& a = P.a;
+  Item I;
+  I.split = (int)(it % a.splits);
+  int64_t rest = it / a.splits;
+  I.hkv = (int)(rest % a.Hkv);
+  rest /= a.Hkv;
+  I.n = (int)(rest % a.N);
+  I.r = (int)(rest / a.N);
+  const int64_t seq = a.seq_lens ? (int64_t)a.seq_lens[I.n] : (int64_t)a.W * a.Lloc;
+  int64_t valid = dcp_local_filled(seq, a.W, a.I, a.I, I.r);
+  if (valid > a.Lloc) valid = a.Lloc;
+  I.t0 = (int64_t)I.split * a.chunk;
+  I.ntok = valid - I.t0;
+  if (I.ntok > a.chunk) I.ntok = a.chunk;
+  if (I.ntok < 0) I.ntok = 0;
+  I.row0 = (((int64_t)I.r * a.N + I.n) * a.Hkv + I.hkv) * a.Lloc + I.t0;
+  return I;
+}
+
+// byte offset of (token, 16-byte chunk) inside a 128B-swizzled [128 x 64] box
+__device__ __forceinline__ uint32_t sw128(int tok, int chunk) {
+  return (uint32_t)(tok * 128 + ((chunk ^ (tok & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                  const DecParams P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = (uint64_t*)(smem + kSmemBar);
+  auto full = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty = [&](int s) { return smem_u32(&bars[kStages + s]); };
+  const uint32_t merge_bar = smem_u32(&bars[2 * kStages]);
+  volatile int* abort_flag = (volatile int*)(smem + kSmemAbort);
+  float* mo = (float*)(smem + kSmemMergeO);
+  float* mml = (float*)(smem + kSmemMergeML);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const DecodeArgs& a = P.a;
+  unsigned* err = a.err;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), kConsumerWarps);
+    }
+    mbar_init(merge_bar, kConsumerWarps);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      prefetch_tensormap(&tk);
+      prefetch_tensormap(&tv);
+      const uint64_t policy = l2_policy_evict_first();
+      uint64_t pos = 0;
+      bool ok = true;
+      for (int64_t it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
+        const Item I = item_of(P, it);
+        const int nst = (int)((I.ntok + kTok - 1) / kTok);
+        for (int st = 0; st < nst; ++st) {
+          const int slot = (int)(pos % kStages);
+          ok = mbar_wait(empty(slot), (uint32_t)(((pos / kStages) & 1) ^ 1), abort_flag, err);
+          if (!ok) break;
+          mbar_arrive_expect_tx(full(slot), kStageBytes);
+          const int row = (int)(I.row0 + (int64_t)st * kTok);
+          const uint32_t dst = sbase + kSmemStages + slot * kStageBytes;
+          tma_load_2d_hint(dst + 0 * kBox, &tk, full(slot), 0, row, policy);
+          tma_load_2d_hint(dst + 1 * kBox, &tk, full(slot), 64, row, policy);
+          tma_load_2d_hint(dst + 2 * kBox, &tv, full(slot), 0, row, policy);
+          tma_load_2d_hint(dst + 3 * kBox, &tv, full(slot), 64, row, policy);
+          ++pos;
+        }
+      }
+      if (!ok) {
+        for (uint64_t p = pos > kStages ? pos - kStages : 0; p < pos; ++p) {
+          volatile int never = 0;
+          mbar_wait(full((int)(p % kStages)), (uint32_t)((p / kStages) & 1), &never, err);
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int g = lane >> 2, t = lane & 3;  // fragment row / column group
+    const int G = P.G;
+    uint64_t pos = 0;
+    uint32_t merges = 0;  // phases completed on merge_bar
+    bool ok = true;
+    for (int64_t it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
+      const Item I = item_of(P, it);
+      const int pidx = I.r * a.splits + I.split;
+      const int64_t R = (int64_t)a.N * a.Hq;
+      const int64_t orow0 = (int64_t)I.n * a.Hq + (int64_t)I.hkv * G;  // first q head row
+      if (I.ntok == 0) {
+        for (int idx = threadIdx.x; idx < G * kD; idx += kConsumerWarps * 32) {
+          const int h = idx / kD, d = idx % kD;
+          a.o_parts[((int64_t)pidx * R + orow0 + h) * kD + d] = 0.f;
+          if (d == 0) a.lse_parts[(int64_t)pidx * R + orow0 + h] = -INFINITY;
+        }
+        continue;
+      }
+      // Q^T operand fragments (B of S^T = K Q^T): head g, d = 16kk + 2t (+8)
+      uint32_t qf[kD / 16][2];
+      {
+        const __nv_bfloat16* qh = (const __nv_bfloat16*)a.q + (orow0 + g) * kD;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          qf[kk][0] = g < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * t) : 0u;
+          qf[kk][1] = g < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * t) : 0u;
+        }
+      }
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      float acc[kD / 16][4];
+#pragma unroll
+      for (int mb = 0; mb < kD / 16; ++mb) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.f;
+
+      const int nst = (int)((I.ntok + kTok - 1) / kTok);
+      for (int st = 0; st < nst; ++st) {
+        const int slot = (int)(pos % kStages);
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(full(slot), (uint32_t)((pos / kStages) & 1), abort_flag, err));
+        if (!ok) break;
+        const uint32_t kb = sbase + kSmemStages + slot * kStageBytes;
+        const uint32_t vb = kb + 2 * kBox;
+        const int64_t base = (int64_t)st * kTok;
+        const int wt = warp * 32;  // first token of this warp in the stage
+        const int64_t nvalid = I.ntok - base;  // valid tokens in this stage (may exceed 128)
+        bool wrote = false;
+        if (nvalid < wt + 32) {
+          // zero the V rows past the valid slots: unused cache slots may hold
+          // any bit pattern, and 0 * NaN would poison the accumulators
+          const int first = (int)max((int64_t)wt, nvalid);
+          const int nrows = wt + 32 - first;
+          uint8_t* vrow = smem + kSmemStages + slot * kStageBytes + 2 * kBox;
+          for (int idx = lane; idx < nrows * 16; idx += 32) {
+            const int tok = first + idx / 16, part = idx % 16;
+            *reinterpret_cast<uint4*>(vrow + (part / 8) * kBox + tok * 128 + (part % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          wrote = true;
+          __syncwarp();
+        }
+#pragma unroll 1
+        for (int gi = 0; gi < 2; ++gi) {
+          const int tb = wt + 16 * gi;
+          if (tb >= nvalid) break;
+          float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const int tok = tb + (lane & 7) + 8 * ((lane >> 3) & 1);
+            const int ch = 2 * kk + (lane >> 4);  // 16-byte chunk along D (0..15)
+            uint32_t af[4];
+            ldsm_x4(kb + (ch >> 3) * kBox + sw128(tok, ch & 7), af);
+            mma_bf16(c, af, qf[kk][0], qf[kk][1]);
+          }
+          const bool va = tb + g < nvalid, vb_ = tb + g + 8 < nvalid;
+          const float x0 = va ? c[0] * P.scale_log2 : -INFINITY;
+          const float x1 = va ? c[1] * P.scale_log2 : -INFINITY;
+          const float x2 = vb_ ? c[2] * P.scale_log2 : -INFINITY;
+          const float x3 = vb_ ? c[3] * P.scale_log2 : -INFINITY;
+          float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+          }
+          if (mx0 > m0 + 8.f || (m0 == -INFINITY && mx0 != -INFINITY)) {
+            const float f = m0 == -INFINITY ? 0.f : ex2(m0 - mx0);
+            l0 *= f;
+#pragma unroll
+            for (int mb = 0; mb < kD / 16; ++mb) {
+              acc[mb][0] *= f;
+              acc[mb][2] *= f;
+            }
+            m0 = mx0;
+          }
+          if (mx1 > m1 + 8.f || (m1 == -INFINITY && mx1 != -INFINITY)) {
+            const float f = m1 == -INFINITY ? 0.f : ex2(m1 - mx1);
+            l1 *= f;
+#pragma unroll
+            for (int mb = 0; mb < kD / 16; ++mb) {
+              acc[mb][1] *= f;
+              acc[mb][3] *= f;
+            }
+            m1 = mx1;
+          }
+          const float r0 = m0 == -INFINITY ? 0.f : m0;
+          const float r1 = m1 == -INFINITY ? 0.f : m1;
+          const float p0 = ex2(x0 - r0), p1 = ex2(x1 - r1), p2 = ex2(x2 - r0), p3 = ex2(x3 - r1);
+          l0 += p0 + p2;
+          l1 += p1 + p3;
+          const uint32_t pb0 = movm_t(pack_bf16x2(p0, p1));
+          const uint32_t pb1 = movm_t(pack_bf16x2(p2, p3));
+#pragma unroll
+          for (int mb = 0; mb < kD / 16; ++mb) {
+            const int q4 = lane >> 3;
+            const int tok = tb + 8 * (q4 >> 1) + (lane & 7);
+            const int ch = 2 * mb + (q4 & 1);
+            uint32_t af[4];
+            ldsm_x4_t(vb + (ch >> 3) * kBox + sw128(tok, ch & 7), af);
+            mma_bf16(acc[mb], af, pb0, pb1);
+          }
+        }
+        // generic-proxy writes to the slot must be ordered before the next
+        // TMA (async proxy) writes into it
+        if (wrote) fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(slot));
+        ++pos;
+      }
+      if (!ok) break;
+      // ------------------------------------------------ merge the four warps
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+      }
+      float* mow = mo + warp * kMaxG * kD;
+      float* mlw = mml + warp * kMaxG * 2;
+      if (lane < 4) {
+        mlw[2 * (2 * t) + 0] = m0;
+        mlw[2 * (2 * t) + 1] = l0;
+        mlw[2 * (2 * t + 1) + 0] = m1;
+        mlw[2 * (2 * t + 1) + 1] = l1;
+      }
+#pragma unroll
+      for (int mb = 0; mb < kD / 16; ++mb) {
+        const int d = 16 * mb + g;
+        mow[(2 * t) * kD + d] = acc[mb][0];
+        mow[(2 * t + 1) * kD + d] = acc[mb][1];
+        mow[(2 * t) * kD + d + 8] = acc[mb][2];
+        mow[(2 * t + 1) * kD + d + 8] = acc[mb][3];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(merge_bar);
+      ok = __all_sync(0xffffffffu, mbar_wait(merge_bar, merges & 1, abort_flag, err));
+      ++merges;
+      if (!ok) break;
+      for (int idx = threadIdx.x; idx < G * kD; idx += kConsumerWarps * 32) {
+        const int h = idx / kD, d = idx % kD;
+        float M = -INFINITY;
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[w * kMaxG * 2 + 2 * h]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float mw = mml[w * kMaxG * 2 + 2 * h];
+            if (mw == -INFINITY) continue;
+            const float f = ex2(mw - M);
+            L += mml[w * kMaxG * 2 + 2 * h + 1] * f;
+            O += mo[(w * kMaxG + h) * kD + d] * f;
+          }
+        }
+        const int64_t prow = (int64_t)pidx * R + orow0 + h;
+        a.o_parts[prow * kD + d] = L > 0.f ? O / L : 0.f;
+        if (d == 0) a.lse_parts[prow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+      }
+      // every warp has read the shared partials before the next item rewrites them
+      __syncwarp();
+      if (lane == 0) mbar_arrive(merge_bar);
+      ok = __all_sync(0xffffffffu, mbar_wait(merge_bar, merges & 1, abort_flag, err));
+      ++merges;
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+void dcp_decode_split(int64_t Lloc, int64_t* chunk, int* splits) {
+  int64_t c = 4096;
+  const int64_t lr = (Lloc + kTok - 1) / kTok * kTok;
+  if (lr < c) c = lr < kTok ? kTok : lr;
+  *chunk = c;
+  *splits = (int)((Lloc + c - 1) / c);
+  if (*splits < 1) *splits = 1;
+}
+
+cudaError_t launch_dcp_decode_partials(const DecodeArgs& a, cudaStream_t stream) {
+  DecParams P;
+  P.a = a;
+  P.G = a.Hq / a.Hkv;
+  P.items = (int64_t)a.W * a.N * a.Hkv * a.splits;
+  P.scale_log2 = a.scale * kLog2e;
+  if (P.items == 0) return cudaSuccess;
+  CUtensorMap tk, tv;
+  const uint64_t rows = (uint64_t)a.W * a.N * a.Hkv * a.Lloc;
+  if (!encode_bf16_2d_sw128(&tk, a.k, rows, kD, kTok, 64) ||
+      !encode_bf16_2d_sw128(&tv, a.v, rows, kD, kTok, 64))
+    return cudaErrorInvalidValue;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(dcp_decode_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  const int sms = device_sm_count();
+  const int64_t grid = P.items < sms ? P.items : sms;
+  dcp_decode_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(tk, tv, P);
+  return cudaGetLastError();
+}
+
+}  // namespace ca

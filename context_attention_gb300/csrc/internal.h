@@ -1,0 +1,71 @@
+// internal.h -- launcher interfaces between the C ABI layer (capi.cu) and the
+// kernel translation units.  Every launcher enqueues on `stream`, performs no
+// host synchronisation and returns the launch's cudaError_t.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ca {
+
+// Geometry and options of one ring-attention launch (fused ring or one
+// partial step).
+struct RingArgs {
+  const void* q;  // [B, Hq, Sq, D]
+  const void* k;  // [B, Hkv, Sk, D]
+  const void* v;
+  int B, Hq, Hkv, D;
+  int64_t Sq, Sk;     // rows per head in the q / k,v tensors
+  int64_t Ls;         // rows per virtual shard
+  int cp;             // ring size (schedule and causal positions)
+  int q_shards;       // shards stored in q (cp for the fused ring, 1 for a step)
+  int q_rank_fixed;   // logical rank of the stored q shard (-1: row r*Ls.. is rank r)
+  int kv_rank_fixed;  // step: logical rank of the stored kv shard; -1: ring over cp
+  int causal, layout, mode;
+  float scale;        // softmax scale
+  const float* c;     // const-max bound [B, Hq, Sq] (natural units) or null
+  void* o;            // output
+  int out_f32;        // 1: fp32 output rows, 0: input dtype (bf16)
+  int unnormalized;   // const-max step: write acc_o instead of acc_o / acc_l
+  float* lse;         // [B, Hq, Sq] or null
+  unsigned* err;      // device error word
+};
+
+cudaError_t launch_ring_tc_bf16(const RingArgs& a, cudaStream_t stream);
+cudaError_t launch_ring_simt_f32(const RingArgs& a, cudaStream_t stream);
+
+cudaError_t launch_const_max_bound(const void* q, const void* k, int is_bf16, int B,
+                                   int Hq, int Hkv, int64_t S, int D, float scale,
+                                   float* c, float* kmax2, cudaStream_t stream);
+
+cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int n,
+                             int64_t R, int D, const float* c, void* o, int out_bf16,
+                             float* lse, cudaStream_t stream);
+
+struct DecodeArgs {
+  const void* q;          // [N, Hq, D] bf16
+  const void* k;          // [W, N, Hkv, Lloc, D] bf16
+  const void* v;
+  int N, Hq, Hkv, D, W, I;
+  int64_t Lloc;
+  const int32_t* seq_lens;  // [N] or null
+  float scale;
+  int splits;             // partials per shard
+  int64_t chunk;          // tokens per split (multiple of 128)
+  float* o_parts;         // [W*splits, N*Hq, D]
+  float* lse_parts;       // [W*splits, N*Hq]
+  unsigned* err;
+};
+cudaError_t launch_dcp_decode_partials(const DecodeArgs& a, cudaStream_t stream);
+// Decode split geometry shared by the workspace query and the launch.
+void dcp_decode_split(int64_t Lloc, int64_t* chunk, int* splits);
+
+cudaError_t launch_permute_rows(const void* src, void* dst, int64_t BH, int64_t S,
+                                int64_t row_bytes, int cp, int layout, int to_shards,
+                                cudaStream_t stream);
+cudaError_t launch_dcp_shard_rows(const void* src, void* dst, int64_t NH, int64_t L,
+                                  int64_t row_bytes, int W, int I, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace ca

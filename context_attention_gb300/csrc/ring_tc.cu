@@ -1,0 +1,548 @@
+// ring_tc.cu -- bf16 ring attention on the 5th-generation tensor cores.
+//
+// What it computes ("Kernel reference: ring_attention_const_max_fwd",
+// sections "Overview", "Design", "Accumulate, then normalize once"; "Sharding
+// the Input" for causal/striped; "DCP (Decode Context Parallelism)" for the
+// LSE form of a partial): the query rows of virtual shard r stay resident
+// while the K/V of shard (r - t) mod cp is visited at ring step t; every
+// step's scores are shifted either by the running row maximum (online max) or
+// by the static per-row bound c_i (const max), exponentiated, summed and
+// multiplied into V, and everything accumulates in fp32 across all steps.
+//
+// How (one GPU, GB300): a persistent kernel, one CTA per SM.  A work unit is
+// 256 query rows (two 128-row tiles) of one (batch, head, shard).  Warp
+// roles:
+//   warps 0-3, 4-7   softmax warpgroups, one per query tile: each thread owns
+//                    one query row (one TMEM lane) -- it reads its S row from
+//                    TMEM, applies mask, shift and exp2, keeps the row sum in
+//                    a register, writes P (bf16) back over S in TMEM, and at
+//                    the end normalises O and writes o and lse;
+//   warp 8           TMA producer: Q tiles, then K and V tiles of every ring
+//                    step in order, through a 5-slot ring of 32 KB buffers;
+//   warp 9           tcgen05 issuer (one thread): S_i = Q_i K^T and
+//                    O_i += P_i V for both tiles, interleaved so that one
+//                    tile's softmax overlaps the other tile's matrix products.
+// TMEM (512 columns): S0, S1 (fp32, 128 each; P aliases their first 64), O0,
+// O1 (fp32, 128 each).  The accumulators never leave TMEM until the unit ends.
+//
+// Online max uses a lazy rescale: a row's reference maximum only moves when
+// the new tile maximum exceeds it by more than 8 (log2 units), so P stays
+// <= 256 and O is rescaled in TMEM only on those rare tiles.  Const max never
+// rescales: merging the ring steps is pure addition.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "index_maps.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace ca {
+namespace {
+
+constexpr int kBM = 128;     // query rows per tile
+constexpr int kBN = 128;     // keys per tile
+constexpr int kD = 128;      // head dimension
+constexpr int kUnitRows = 2 * kBM;
+constexpr int kNSlot = 5;    // K/V ring slots
+constexpr uint32_t kTileBytes = kBM * kD * 2;  // 32 KB
+constexpr uint32_t kBoxBytes = kTileBytes / 2;  // one 64-column half
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+
+constexpr uint32_t kSmemQ = 0;
+constexpr uint32_t kSmemKV = 2 * kTileBytes;
+constexpr uint32_t kSmemBar = kSmemKV + kNSlot * kTileBytes;
+// barrier indices
+constexpr int kBarKvFull = 0;
+constexpr int kBarKvEmpty = kBarKvFull + kNSlot;
+constexpr int kBarQFull = kBarKvEmpty + kNSlot;
+constexpr int kBarQEmpty = kBarQFull + 1;
+constexpr int kBarSFull = kBarQEmpty + 1;   // 2
+constexpr int kBarPFull = kBarSFull + 2;    // 2
+constexpr int kBarOFull = kBarPFull + 2;    // 2
+constexpr int kNumBars = kBarOFull + 2;
+constexpr uint32_t kSmemTmemSlot = kSmemBar + 8 * kNumBars;
+constexpr uint32_t kSmemAbort = kSmemTmemSlot + 4;
+constexpr uint32_t kSmemUsed = kSmemAbort + 4;
+constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // slack for 1024-byte alignment
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;    // + 128*i
+constexpr uint32_t kColO = 256;  // + 128*i
+
+constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, false, true);
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct TcParams {
+  RingArgs a;
+  int qblocks;      // 256-row units per stored q shard
+  int64_t units;    // total work units
+  int64_t per_head; // units per (b, h)
+  int nsteps;
+  int nkt;          // key tiles per shard
+  float scale_log2;
+};
+
+struct Unit {
+  int64_t bh;
+  int b, h;
+  int64_t bhk;
+  int r_store, r_log;
+  int64_t qrow0;  // first local query row of the unit
+};
+
+__device__ __forceinline__ Unit unit_of(const TcParams& P, int64_t u) {
+  Unit U;
+  U.bh = u / P.per_head;
+  // heaviest units of a head first (causal work grows with the shard and row)
+  const int64_t rem = P.per_head - 1 - (u % P.per_head);
+  U.r_store = (int)(rem / P.qblocks);
+  U.qrow0 = (rem % P.qblocks) * kUnitRows;
+  U.b = (int)(U.bh / P.a.Hq);
+  U.h = (int)(U.bh % P.a.Hq);
+  U.bhk = (int64_t)U.b * P.a.Hkv + U.h / (P.a.Hq / P.a.Hkv);
+  U.r_log = P.a.q_rank_fixed >= 0 ? P.a.q_rank_fixed : U.r_store;
+  return U;
+}
+
+// Key tiles of ring step t that can be visible to some row of the unit.
+__device__ __forceinline__ int step_tiles(const TcParams& P, const Unit& U, int t,
+                                          int* s_store, int64_t* delta) {
+  const int s_log = P.a.kv_rank_fixed >= 0 ? P.a.kv_rank_fixed : ring_kv_shard(U.r_log, t, P.a.cp);
+  *s_store = P.a.kv_rank_fixed >= 0 ? 0 : s_log;
+  *delta = P.a.causal ? causal_delta(P.a.layout, U.r_log, s_log) : kDeltaAll;
+  if (*delta == kDeltaNone) return 0;
+  if (*delta == kDeltaAll) return P.nkt;
+  const int64_t a_max = min(U.qrow0 + kUnitRows - 1, P.a.Ls - 1);
+  const int64_t bmax = a_max - *delta;
+  if (bmax < 0) return 0;
+  return (int)min((int64_t)P.nkt, bmax / kBN + 1);
+}
+
+__device__ __forceinline__ int unit_tiles(const TcParams& P, const Unit& U) {
+  int n = 0, s;
+  int64_t d;
+  for (int t = 0; t < P.nsteps; ++t) n += step_tiles(P, U, t, &s, &d);
+  return n;
+}
+
+// Walks the (step, key tile) sequence of a unit in ring order.
+struct TileIter {
+  int t, kt, nk, s_store;
+  int64_t delta;
+  __device__ __forceinline__ void seek(const TcParams& P, const Unit& U) {
+    while (t < P.nsteps) {
+      nk = step_tiles(P, U, t, &s_store, &delta);
+      if (nk > 0) return;
+      ++t;
+    }
+  }
+  __device__ __forceinline__ void begin(const TcParams& P, const Unit& U) {
+    t = 0;
+    kt = 0;
+    seek(P, U);
+  }
+  __device__ __forceinline__ void next(const TcParams& P, const Unit& U) {
+    if (++kt < nk) return;
+    kt = 0;
+    ++t;
+    seek(P, U);
+  }
+};
+
+__device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sbase, int i, int slot) {
+  const uint32_t d = tmem + kColS + 128u * i;
+  const uint32_t qa = sbase + kSmemQ + i * kTileBytes;
+  const uint32_t ka = sbase + kSmemKV + slot * kTileBytes;
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+    tc_mma_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+              kIdescS, kk > 0);
+  }
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int i, int slot,
+                                         bool acc) {
+  const uint32_t d = tmem + kColO + 128u * i;
+  const uint32_t p = tmem + kColS + 128u * i;
+  const uint32_t va = sbase + kSmemKV + slot * kTileBytes;
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    tc_mma_ts(d, p + kk * 8, smem_desc_sw128(va + kk * 2048, kBoxBytes, 1024), kIdescPV,
+              (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const TcParams P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = (uint64_t*)(smem + kSmemBar);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  uint32_t* tmem_slot = (uint32_t*)(smem + kSmemTmemSlot);
+  volatile int* abort_flag = (volatile int*)(smem + kSmemAbort);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  unsigned* err = P.a.err;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < kNSlot; ++s) {
+      mbar_init(bar(kBarKvFull + s), 1);
+      mbar_init(bar(kBarKvEmpty + s), 1);
+    }
+    mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQEmpty), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarSFull + i), 1);
+      mbar_init(bar(kBarPFull + i), kBM);
+      mbar_init(bar(kBarOFull + i), 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tensormap(&tq);
+    prefetch_tensormap(&tk);
+    prefetch_tensormap(&tv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t uc = 0;
+      uint64_t pos = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+        const Unit U = unit_of(P, u);
+        const int n = unit_tiles(P, U);
+        if (n == 0) continue;
+        ok = mbar_wait(bar(kBarQEmpty), (uc & 1) ^ 1, abort_flag, err);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes);
+        const int qrow = (int)(U.bh * P.a.Sq + (int64_t)U.r_store * P.a.Ls + U.qrow0);
+        for (int i = 0; i < 2; ++i)
+          for (int hx = 0; hx < 2; ++hx)
+            tma_load_2d(sbase + kSmemQ + i * kTileBytes + hx * kBoxBytes, &tq, bar(kBarQFull),
+                        hx * 64, qrow + i * kBM);
+        TileIter it;
+        it.begin(P, U);
+        for (int j = 0; j < n && ok; ++j) {
+          const int krow = (int)(U.bhk * P.a.Sk + (int64_t)it.s_store * P.a.Ls + (int64_t)it.kt * kBN);
+          for (int kv = 0; kv < 2 && ok; ++kv) {
+            const int slot = (int)(pos % kNSlot);
+            const uint32_t ph = (uint32_t)((pos / kNSlot) & 1);
+            ok = mbar_wait(bar(kBarKvEmpty + slot), ph ^ 1, abort_flag, err);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(kBarKvFull + slot), kTileBytes);
+            const CUtensorMap* m = kv == 0 ? &tk : &tv;
+            for (int hx = 0; hx < 2; ++hx)
+              tma_load_2d(sbase + kSmemKV + slot * kTileBytes + hx * kBoxBytes, m,
+                          bar(kBarKvFull + slot), hx * 64, krow);
+            ++pos;
+          }
+          it.next(P, U);
+        }
+        ++uc;
+      }
+      if (!ok) {
+        // error path: let the copies already in flight land before exit
+        for (uint64_t p = pos > kNSlot ? pos - kNSlot : 0; p < pos; ++p) {
+          volatile int never = 0;
+          mbar_wait(bar(kBarKvFull + (int)(p % kNSlot)), (uint32_t)((p / kNSlot) & 1), &never, err);
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t uc = 0;
+      uint64_t pos = 0, gt = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+        const Unit U = unit_of(P, u);
+        const int n = unit_tiles(P, U);
+        if (n == 0) continue;
+        ok = mbar_wait(bar(kBarQFull), uc & 1, abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        int kslot = (int)(pos % kNSlot);
+        ok = mbar_wait(bar(kBarKvFull + kslot), (uint32_t)((pos / kNSlot) & 1), abort_flag, err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(tmem, sbase, 0, kslot);
+        tc_commit(bar(kBarSFull + 0));
+        issue_s(tmem, sbase, 1, kslot);
+        tc_commit(bar(kBarSFull + 1));
+        if (n == 1) tc_commit(bar(kBarQEmpty));
+        tc_commit(bar(kBarKvEmpty + kslot));
+        ++pos;
+        for (int j = 0; j < n && ok; ++j) {
+          const int vslot = (int)(pos % kNSlot);
+          ok = mbar_wait(bar(kBarKvFull + vslot), (uint32_t)((pos / kNSlot) & 1), abort_flag, err);
+          if (!ok) break;
+          const uint32_t pph = (uint32_t)((gt + j) & 1);
+          ok = mbar_wait(bar(kBarPFull + 0), pph, abort_flag, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(tmem, sbase, 0, vslot, j > 0);
+          ++pos;
+          const bool more = j + 1 < n;
+          if (more) {
+            kslot = (int)(pos % kNSlot);
+            ok = mbar_wait(bar(kBarKvFull + kslot), (uint32_t)((pos / kNSlot) & 1), abort_flag, err);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(tmem, sbase, 0, kslot);
+            tc_commit(bar(kBarSFull + 0));
+          } else {
+            tc_commit(bar(kBarOFull + 0));
+          }
+          ok = mbar_wait(bar(kBarPFull + 1), pph, abort_flag, err);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(tmem, sbase, 1, vslot, j > 0);
+          tc_commit(bar(kBarKvEmpty + vslot));
+          if (more) {
+            issue_s(tmem, sbase, 1, kslot);
+            tc_commit(bar(kBarSFull + 1));
+            if (j + 1 == n - 1) tc_commit(bar(kBarQEmpty));
+            tc_commit(bar(kBarKvEmpty + kslot));
+            ++pos;
+          } else {
+            tc_commit(bar(kBarOFull + 1));
+          }
+        }
+        gt += n;
+        ++uc;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int i = warp / 4;                 // query tile of this warpgroup
+    const int quarter = warp % 4;           // TMEM lane quarter
+    const int tid = quarter * 32 + lane;    // row within the tile
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_base + kColS + 128u * i;
+    const uint32_t tO = tmem + lane_base + kColO + 128u * i;
+    const bool const_max = P.a.mode == 1;
+    uint32_t uc = 0;
+    uint64_t gt = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+      const Unit U = unit_of(P, u);
+      const int n = unit_tiles(P, U);
+      const int64_t a_row = U.qrow0 + (int64_t)i * kBM + tid;
+      const bool valid = a_row < P.a.Ls;
+      const int64_t orow = U.bh * P.a.Sq + (int64_t)U.r_store * P.a.Ls + a_row;
+      if (n == 0) {
+        if (valid) {
+          if (P.a.out_f32) {
+            float4* dst = (float4*)((float*)P.a.o + orow * kD);
+            for (int c = 0; c < kD / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          } else {
+            uint4* dst = (uint4*)((__nv_bfloat16*)P.a.o + orow * kD);
+            for (int c = 0; c < kD / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+          }
+          if (P.a.lse) P.a.lse[orow] = -INFINITY;
+        }
+        continue;
+      }
+      float c_nat = 0.f;
+      if (const_max && valid) c_nat = P.a.c[orow];
+      const float c_log2 = c_nat * kLog2e;
+      float m = -INFINITY;  // reference max, log2 units (online mode)
+      float l = 0.f;
+      TileIter it;
+      it.begin(P, U);
+      for (int j = 0; j < n; ++j) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar(kBarSFull + i), (uint32_t)((gt + j) & 1), abort_flag, err));
+        if (!ok) break;
+        tc_fence_after();
+        // last visible column of this tile for this row
+        const int64_t b0 = (int64_t)it.kt * kBN;
+        int64_t lim = P.a.Ls - 1 - b0;
+        if (it.delta != kDeltaAll) lim = min(lim, a_row - it.delta - b0);
+        const int vis_max = (int)max((int64_t)-1, min(lim, (int64_t)(kBN - 1)));
+        const bool need_mask = __any_sync(0xffffffffu, vis_max < kBN - 1);
+        float mref;
+        if (const_max) {
+          mref = c_log2;
+        } else {
+          // pass 1: row maximum straight from TMEM, 32 columns at a time
+          float mx = -INFINITY;
+#pragma unroll
+          for (int ch = 0; ch < kBN / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld32(tS + ch * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+              const float v = (need_mask && ch * 32 + x > vis_max) ? -INFINITY : __uint_as_float(r[x]);
+              mx = fmaxf(mx, v);
+            }
+          }
+          mx *= P.scale_log2;
+          float fac = 1.f;
+          bool need_o = false;
+          if (mx > m + kRescaleThreshold || (m == -INFINITY && mx != -INFINITY)) {
+            fac = (m == -INFINITY) ? 0.f : ex2(m - mx);
+            need_o = (m != -INFINITY) && (j > 0);
+            l *= fac;
+            m = mx;
+          }
+          if (__any_sync(0xffffffffu, need_o)) {
+            const float f = need_o ? fac : 1.f;
+#pragma unroll 1
+            for (int ch = 0; ch < kD / 32; ++ch) {
+              uint32_t r[32];
+              tmem_ld32(tO + ch * 32, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * f);
+              tmem_st32(tO + ch * 32, r);
+            }
+            tmem_st_wait();
+          }
+          mref = (m == -INFINITY) ? 0.f : m;
+        }
+        // pass 2: p = 2^(s*scale*log2e - ref), row sum, bf16 P written over
+        // the S columns already consumed (P column block ch < S block ch+1)
+        float psum = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < kBN / 32; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(tS + ch * 32, r);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            float s0 = __uint_as_float(r[2 * x]), s1 = __uint_as_float(r[2 * x + 1]);
+            if (need_mask) {
+              if (ch * 32 + 2 * x > vis_max) s0 = -INFINITY;
+              if (ch * 32 + 2 * x + 1 > vis_max) s1 = -INFINITY;
+            }
+            const float p0 = ex2(fmaf(s0, P.scale_log2, -mref));
+            const float p1 = ex2(fmaf(s1, P.scale_log2, -mref));
+            psum += p0 + p1;
+            pk[x] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + ch * 16, pk);
+        }
+        l += psum;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPFull + i));
+        it.next(P, U);
+      }
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + i), uc & 1, abort_flag, err));
+      if (!ok) break;
+      tc_fence_after();
+      float inv, lse;
+      if (const_max) {
+        inv = P.a.unnormalized ? 1.f : 1.f / fmaxf(l, 1e-37f);
+        lse = c_nat + logf(l);
+      } else if (l > 0.f) {
+        inv = 1.f / l;
+        lse = (m + log2f(l)) * kLn2;
+      } else {
+        inv = 0.f;
+        lse = -INFINITY;
+      }
+#pragma unroll
+      for (int ch = 0; ch < kD / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(tO + ch * 32, r);
+        tmem_ld_wait();
+        if (valid) {
+          if (P.a.out_f32) {
+            float4* dst = (float4*)((float*)P.a.o + orow * kD + ch * 32);
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              dst[x] = make_float4(__uint_as_float(r[4 * x]) * inv, __uint_as_float(r[4 * x + 1]) * inv,
+                                   __uint_as_float(r[4 * x + 2]) * inv, __uint_as_float(r[4 * x + 3]) * inv);
+          } else {
+            uint4* dst = (uint4*)((__nv_bfloat16*)P.a.o + orow * kD + ch * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              uint32_t w[4];
+#pragma unroll
+              for (int y = 0; y < 4; ++y)
+                w[y] = pack_bf16x2(__uint_as_float(r[8 * x + 2 * y]) * inv,
+                                   __uint_as_float(r[8 * x + 2 * y + 1]) * inv);
+              dst[x] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+      if (valid && P.a.lse) P.a.lse[orow] = lse;
+      gt += n;
+      ++uc;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ring_tc_bf16(const RingArgs& a, cudaStream_t stream) {
+  if (a.D != kD) return cudaErrorInvalidValue;
+  TcParams P;
+  P.a = a;
+  P.qblocks = (int)((a.Ls + kUnitRows - 1) / kUnitRows);
+  P.per_head = (int64_t)a.q_shards * P.qblocks;
+  P.units = (int64_t)a.B * a.Hq * P.per_head;
+  P.nsteps = a.kv_rank_fixed >= 0 ? 1 : a.cp;
+  P.nkt = (int)((a.Ls + kBN - 1) / kBN);
+  P.scale_log2 = a.scale * kLog2e;
+  if (P.units == 0) return cudaSuccess;
+
+  CUtensorMap tq, tk, tv;
+  if (!encode_bf16_2d_sw128(&tq, a.q, (uint64_t)a.B * a.Hq * a.Sq, kD, kBM, 64) ||
+      !encode_bf16_2d_sw128(&tk, a.k, (uint64_t)a.B * a.Hkv * a.Sk, kD, kBN, 64) ||
+      !encode_bf16_2d_sw128(&tv, a.v, (uint64_t)a.B * a.Hkv * a.Sk, kD, kBN, 64))
+    return cudaErrorInvalidValue;
+
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(ring_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  const int sms = device_sm_count();
+  const int64_t grid = P.units < sms ? P.units : sms;
+  ring_tc_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(tq, tk, tv, P);
+  return cudaGetLastError();
+}
+
+}  // namespace ca

@@ -1,0 +1,283 @@
+/*
+ * ctxattn.h -- C ABI of libctxattn.so: the hot path of context-parallel
+ * attention on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (web pages on context parallelism):
+ *   [CM]   "Kernel reference: ring_attention_const_max_fwd const-max ring
+ *          attention" (Neuron docs, vllm-omni-neuron).
+ *   [DCP]  "DCP (Decode Context Parallelism)" (Neuron docs, vllm-neuron).
+ *   [CP]   "Context Parallelism in vLLM Omni Neuron" (Neuron docs).
+ *   [SHI]  "Sharding the Input" (iop.systems blog).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers marked "device" are CUDA device (or managed) addresses of the
+ *   current device; pointers marked "host" are host addresses.  The caller
+ *   owns and allocates every buffer, workspace included.  The library never
+ *   allocates, frees or synchronises; device work is enqueued on `stream`
+ *   (a cudaStream_t passed as void*, NULL = legacy default stream).
+ * - Tensors are dense row-major, no strides.  Element types: CA_DTYPE_BF16
+ *   (inputs and outputs bf16, all accumulation fp32) or CA_DTYPE_F32 (fp32
+ *   end to end).  LSE values are fp32, natural log, softmax scale included:
+ *   lse_i = ln sum_j exp(scale * q_i . k_j).
+ * - Attention tensors: q is [B, Hq, S, D]; k and v are [B, Hkv, S, D]; query
+ *   head h reads key/value head h / (Hq / Hkv) (consecutive groups).
+ * - Virtual shards: the S rows of a head are `cp_size` shards of Ls = S /
+ *   cp_size rows, stored shard-major: row r*Ls + a is local token a of shard
+ *   r.  Its global position is r*Ls + a (CA_LAYOUT_CONTIGUOUS, [CP] "Model
+ *   Implementation": start = cp_rank * local_S) or a*cp_size + r
+ *   (CA_LAYOUT_STRIPED, [SHI]: token t on shard t mod cp).  Outputs use the
+ *   same row order as q.
+ * - Causal: key j is visible to query i iff global(j) <= global(i).
+ * - Errors: every call validates its arguments on the host first and returns
+ *   a ca_status; on a host-side error nothing is enqueued and nothing is
+ *   written.  There is no fallback path: an unsupported case is an error.
+ *   CA_ERR_CUDA reports a failed launch (cudaGetLastError after the launch).
+ *   Device-side faults of the bounded waits are reported by
+ *   ca_device_status().
+ * - Supported: bf16 with D = 128; fp32 with 1 <= D <= 128.  Device: compute
+ *   capability 10.3 (GB300) for the bf16 kernels; the fp32 and
+ *   data-movement kernels run on the same build (sm_103a).
+ */
+#ifndef CTXATTN_H
+#define CTXATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CA_OK = 0,
+  CA_ERR_INVALID_ARG = 1, /* null pointer, bad enum, non-positive size */
+  CA_ERR_SHAPE = 2,       /* S % cp_size != 0, Hq % Hkv != 0, bad shard sizes */
+  CA_ERR_UNSUPPORTED = 3, /* dtype/D combination or device not supported */
+  CA_ERR_ALIGNMENT = 4,   /* a device pointer is not 16-byte aligned */
+  CA_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required */
+  CA_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed */
+  CA_ERR_TIMEOUT = 7      /* a bounded device-side wait gave up */
+} ca_status;
+
+typedef enum { CA_DTYPE_F32 = 0, CA_DTYPE_BF16 = 1 } ca_dtype;
+typedef enum { CA_MODE_ONLINE_MAX = 0, CA_MODE_CONST_MAX = 1 } ca_mode;
+typedef enum { CA_LAYOUT_CONTIGUOUS = 0, CA_LAYOUT_STRIPED = 1 } ca_layout;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *ca_status_string(ca_status status);
+
+/* Library ABI version (major*100 + minor). */
+int ca_version(void);
+
+/* ------------------------------------------------------------------------
+ * Ring attention forward ([CM] "Overview", "Design", "Interface").
+ *
+ * Q stays resident; the K/V of the cp_size virtual shards are visited one
+ * ring step at a time: the query rows of shard r meet, at step t = 0 ..
+ * cp_size-1, the keys of shard (r - t) mod cp_size.  Every step's partial
+ * result is folded into an fp32 accumulator that never leaves the SM.
+ *   mode CA_MODE_ONLINE_MAX: flash-style running row maximum; folding a step
+ *     is the LSE merge w_i = exp(lse_i - lse_global) ([DCP] "Decode Compute
+ *     Pattern", steps 4-7) applied tile by tile.
+ *   mode CA_MODE_CONST_MAX: the per-row Cauchy-Schwarz bound
+ *     c_i = scale * |q_i| * max_j |k_j| (max over all S keys of the key/value
+ *     head, [CM] "Picking a max that is safe without measuring it") replaces
+ *     the running max; steps merge by pure addition of unnormalised sums and
+ *     the row is normalised once, o = acc_o / max(acc_l, 1e-37), lse =
+ *     c + ln(acc_l) ([CM] "A static bound makes the ring reduction pure
+ *     addition", "Accumulate, then normalize once").  Rows whose bound
+ *     overshoots the true row maximum by more than ~87 nats underflow to the
+ *     clamp, exactly as the page warns ("Common issues").
+ *
+ * q, k, v     device, [B,Hq,S,D] / [B,Hkv,S,D], dtype, 16-byte aligned.
+ * o           device, [B,Hq,S,D], dtype (same row order as q).
+ * lse         device, [B,Hq,S] fp32, or NULL.
+ * softmax_scale  <= 0 selects 1/sqrt(D).
+ * workspace   device, at least ca_ring_attn_fwd_workspace_size() bytes
+ *             (may be NULL when that size is 0).
+ * Errors: CA_ERR_SHAPE if S % cp_size != 0 ([CP] "Sequence Length
+ * Constraints": S=3645 with cp_size=8 is rejected) or Hq % Hkv != 0;
+ * CA_ERR_UNSUPPORTED for bf16 with D != 128.
+ * ---------------------------------------------------------------------- */
+size_t ca_ring_attn_fwd_workspace_size(int B, int Hq, int Hkv, int64_t S, int D,
+                                       int cp_size, ca_mode mode);
+ca_status ca_ring_attn_fwd(const void *q, const void *k, const void *v, void *o,
+                           float *lse, ca_dtype dtype, int B, int Hq, int Hkv,
+                           int64_t S, int D, int cp_size, ca_mode mode,
+                           int causal, ca_layout layout, float softmax_scale,
+                           void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/* Ring attention in const-max mode with a caller-provided bound
+ * c [B,Hq,S] fp32 (device; e.g. from ca_const_max_bound): the same
+ * computation as ca_ring_attn_fwd(mode = CA_MODE_CONST_MAX) without the bound
+ * pass, for callers that compute or reuse the bound themselves.  Needs no
+ * workspace. */
+ca_status ca_ring_attn_fwd_bounded(const void *q, const void *k, const void *v,
+                                   const float *c, void *o, float *lse,
+                                   ca_dtype dtype, int B, int Hq, int Hkv,
+                                   int64_t S, int D, int cp_size, int causal,
+                                   ca_layout layout, float softmax_scale,
+                                   void *stream);
+
+/* ------------------------------------------------------------------------
+ * One ring step ([CM] "Overview", step t: acc_r += attn(Q_r, K_{r-t},
+ * V_{r-t})): the queries of shard q_rank against the keys of shard kv_rank
+ * only, with the causal rule evaluated on global positions of the given
+ * layout.
+ *
+ * q_shard     device [B,Hq,Ls,D]; k_shard, v_shard device [B,Hkv,Ls,D].
+ * c           CA_MODE_CONST_MAX: device [B,Hq,Ls] fp32 bound rows of this
+ *             shard (from ca_const_max_bound); CA_MODE_ONLINE_MAX: NULL.
+ * o_part      device [B,Hq,Ls,D] fp32.  Online max: the normalised partial
+ *             o_i.  Const max: the unnormalised sum acc_o = sum_j
+ *             exp(s_ij - c_i) v_j.
+ * lse_part    device [B,Hq,Ls] fp32: the partial's log-sum-exp (both modes;
+ *             in const max it is c_i + ln acc_l).  A row with no visible key
+ *             gets o_part = 0 and lse_part = -inf.
+ * ---------------------------------------------------------------------- */
+ca_status ca_attn_partial_step(const void *q_shard, const void *k_shard,
+                               const void *v_shard, ca_dtype dtype, int B,
+                               int Hq, int Hkv, int64_t Ls, int D, int q_rank,
+                               int kv_rank, int cp_size, ca_mode mode,
+                               int causal, ca_layout layout,
+                               float softmax_scale, const float *c,
+                               float *o_part, float *lse_part, void *stream);
+
+/* ------------------------------------------------------------------------
+ * LSE merge of n partial results ([DCP] "Decode Compute Pattern" steps 5-7
+ * and "Segmented Attention CP" step 6; [CM] "Accumulate, then normalize
+ * once").
+ *
+ * o_parts     device [n, R, D] fp32; lse_parts device [n, R] fp32.
+ * c == NULL:  partials are normalised; L = ln sum_i exp(lse_i),
+ *             o = sum_i exp(lse_i - L) o_i.  Partials with lse = -inf get
+ *             weight 0; if all are -inf the row gets o = 0, lse = -inf.
+ * c != NULL:  device [R] fp32 bound; partials are the unnormalised const-max
+ *             sums of ca_attn_partial_step; acc_l_i = exp(lse_i - c),
+ *             o = sum_i o_i / max(sum_i acc_l_i, 1e-37), lse = c + ln sum_i
+ *             acc_l_i (pure addition).
+ * o           device [R, D] of out_dtype; lse device [R] fp32 or NULL.
+ * ---------------------------------------------------------------------- */
+ca_status ca_lse_merge(const float *o_parts, const float *lse_parts, int n,
+                       int64_t R, int D, const float *c, void *o,
+                       ca_dtype out_dtype, float *lse, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Const-max bound ([CM] "Picking a max ...", "Global key max", "Assembling
+ * the bound"): kmax2[b,hk] = max_j |k_j|^2 over all S rows of the head, then
+ * c[b,h,i] = sqrt(scale^2 * kmax2[b,h/G] * |q_i|^2) (one square root per row).
+ *
+ * q, k        device, [B,Hq,S,D] / [B,Hkv,S,D], dtype.
+ * c           device [B,Hq,S] fp32 (output).
+ * kmax2       device [B,Hkv] fp32 (output; also the reduction target).
+ * ---------------------------------------------------------------------- */
+ca_status ca_const_max_bound(const void *q, const void *k, ca_dtype dtype,
+                             int B, int Hq, int Hkv, int64_t S, int D,
+                             float softmax_scale, float *c, float *kmax2,
+                             void *stream);
+
+/* ------------------------------------------------------------------------
+ * DCP decode ([DCP] "DCP Decode", "Decode Compute Pattern", "local_filled
+ * Computation"): one query token per sequence against K/V shards whose
+ * blocks of `interleave` tokens are dealt round robin to dcp ranks (block b
+ * on rank b mod dcp, [DCP] "Slot Mapping and KV Cache").  Each rank's local
+ * slots [0, local_filled(seq_len, rank)) are valid; every rank computes a
+ * partial (o_r, lse_r) and the partials are LSE-merged.
+ *
+ * q           device [N, Hq, D], dtype.
+ * k_shards, v_shards  device [dcp, N, Hkv, Lloc, D], dtype.
+ * seq_lens    device int32 [N] (tokens in the cache, 0..dcp*Lloc), or NULL
+ *             for dcp*Lloc everywhere.
+ * o           device [N, Hq, D], dtype; lse device [N, Hq] fp32 (or NULL).
+ * workspace   device, ca_dcp_decode_workspace_size() bytes (partials).
+ * Errors: CA_ERR_SHAPE if Hq % Hkv != 0 or Lloc % interleave != 0;
+ * CA_ERR_UNSUPPORTED unless bf16 with D = 128 and Hq/Hkv <= 8.
+ * ---------------------------------------------------------------------- */
+size_t ca_dcp_decode_workspace_size(int N, int Hq, int Hkv, int64_t Lloc,
+                                    int D, int dcp, int interleave);
+ca_status ca_dcp_decode(const void *q, const void *k_shards,
+                        const void *v_shards, ca_dtype dtype, int N, int Hq,
+                        int Hkv, int64_t Lloc, int D, int dcp, int interleave,
+                        const int32_t *seq_lens, float softmax_scale, void *o,
+                        float *lse, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/* ------------------------------------------------------------------------
+ * Device layout permutations (bit-exact copies of rows of row_bytes bytes).
+ *
+ * ca_layout_to_shards: x holds BH heads of S rows in global token order;
+ *   y receives them shard-major for `layout` (y row r*Ls + a = x row
+ *   global(r, a)).  ca_layout_from_shards is the inverse.
+ * ca_dcp_shard_kv: kv holds NH heads of L rows in global token order; shards
+ *   receives [dcp, NH, L/dcp] rows, global position p going to rank
+ *   (p / interleave) mod dcp at its local slot ([DCP] "Slot Mapping and KV
+ *   Cache", "Segmented Attention CP": slot s of rank R is global
+ *   (s / I)*(dcp*I) + R*I + s % I).  Requires L % (dcp*interleave) == 0.
+ * row_bytes must be a multiple of 16; pointers 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+ca_status ca_layout_to_shards(const void *x, void *y, int64_t BH, int64_t S,
+                              int64_t row_bytes, int cp_size, ca_layout layout,
+                              void *stream);
+ca_status ca_layout_from_shards(const void *y, void *x, int64_t BH, int64_t S,
+                                int64_t row_bytes, int cp_size,
+                                ca_layout layout, void *stream);
+ca_status ca_dcp_shard_kv(const void *kv, void *shards, int64_t NH, int64_t L,
+                          int64_t row_bytes, int dcp, int interleave,
+                          void *stream);
+
+/* ------------------------------------------------------------------------
+ * Host index helpers (pure functions, no CUDA calls).  The kernels use the
+ * same closed forms on the device.
+ * ---------------------------------------------------------------------- */
+
+/* Global token position of stored row `row` (= r*Ls + a) for `layout`;
+ * -1 on bad arguments. */
+int64_t ca_layout_global_index(ca_layout layout, int cp_size, int64_t Ls,
+                               int64_t row);
+/* Inverse: stored row of global token `token`; -1 on bad arguments. */
+int64_t ca_layout_shard_row(ca_layout layout, int cp_size, int64_t Ls,
+                            int64_t token);
+/* Ring schedule ([CM] "Overview"): K/V shard met by shard `rank` at `step`,
+ * (rank - step) mod cp_size; -1 on bad arguments. */
+int ca_ring_kv_shard(int rank, int step, int cp_size);
+
+/* Owner rank of global position pos: (pos / interleave) mod dcp. */
+int ca_dcp_owner(int64_t pos, int dcp, int interleave);
+/* Local slot of pos on its owner: (pos / (dcp*I))*I + pos % I. */
+int64_t ca_dcp_local_index(int64_t pos, int dcp, int interleave);
+/* Global position of local slot s on rank R ([DCP] "Segmented Attention
+ * CP"): (s / I)*(dcp*I) + R*I + s % I. */
+int64_t ca_dcp_local_to_global(int64_t local, int rank, int dcp,
+                               int interleave);
+/* Tokens among positions [0, N) held by rank R: the [DCP] "local_filled
+ * Computation" formula, evaluated as printed (block_size = the KV block size;
+ * the pages require it to equal interleave). -1 on bad arguments. */
+int64_t ca_dcp_local_filled(int64_t N, int dcp, int interleave, int block_size,
+                            int rank);
+/* [DCP] "Active Token Handling": 1 if rank owns the token at position N
+ * (the decoded token), else 0; -1 on bad arguments. */
+int ca_dcp_active_mask(int64_t N, int dcp, int interleave, int block_size,
+                       int rank);
+/* [DCP] "Slot Mapping and KV Cache": for each position, -1 unless `rank`
+ * owns it, else block_table[p / (block_size*dcp)] * block_size + the
+ * position's offset among the rank's tokens of that virtual block.
+ * positions, block_table, slots: host arrays. */
+ca_status ca_dcp_slot_mapping(const int64_t *positions, int64_t n,
+                              const int32_t *block_table, int64_t n_blocks,
+                              int block_size, int dcp, int rank,
+                              int interleave, int64_t *slots);
+
+/* ------------------------------------------------------------------------
+ * Device status: reads (synchronously, on the current device) the error word
+ * that bounded waits set when they give up, and clears it if `reset`.
+ * Returns CA_OK, CA_ERR_TIMEOUT, or CA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+ca_status ca_device_status(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CTXATTN_H */

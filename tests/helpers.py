@@ -1,0 +1,72 @@
+"""Shared helpers for the GPU parity tests: tolerances and oracle sampling."""
+import numpy as np
+import torch
+
+import oracle
+
+# Tolerances fixed for this hot path: bf16 inputs with fp32 accumulation,
+# fp32 inputs, LSE (natural log).
+BF16_MAX_ABS = 2e-2
+BF16_MEAN_ABS = 2e-3
+F32_MAX_ABS = 1e-4
+LSE_ABS = 1e-3
+
+
+def np32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy()
+
+
+def assert_close(gpu_o, ref_o, gpu_lse=None, ref_lse=None, dtype=torch.bfloat16, what=""):
+    g = np.asarray(gpu_o, dtype=np.float64).reshape(np.asarray(ref_o).shape)
+    err = np.abs(g - ref_o)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    if dtype == torch.bfloat16:
+        assert err.max() <= BF16_MAX_ABS, f"{what}: max abs err {err.max():.3e}"
+        assert err.mean() <= BF16_MEAN_ABS, f"{what}: mean abs err {err.mean():.3e}"
+    else:
+        assert err.max() <= F32_MAX_ABS, f"{what}: max abs err {err.max():.3e}"
+    if gpu_lse is not None:
+        gl = np.asarray(gpu_lse, dtype=np.float64).reshape(np.asarray(ref_lse).shape)
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(fin, np.isfinite(gl)), f"{what}: -inf pattern of lse differs"
+        if fin.any():
+            le = np.abs(gl[fin] - ref_lse[fin]).max()
+            assert le <= LSE_ABS, f"{what}: lse err {le:.3e}"
+    return err.max(), err.mean()
+
+
+def sample_rows(B, H, S, cp, n_per_head, seed, heads=None):
+    """Seeded sample of (b, h, rho) rows: every shard's first and last row,
+    plus random rows; returns {(b, h): sorted rho array}."""
+    rng = np.random.default_rng(seed)
+    Ls = S // cp
+    out = {}
+    pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
+    for b, h in pairs:
+        fixed = [r * Ls for r in range(cp)] + [r * Ls + Ls - 1 for r in range(cp)]
+        rnd = rng.integers(0, S, size=max(0, n_per_head - len(fixed)))
+        out[(b, h)] = np.unique(np.concatenate([fixed, rnd]).astype(np.int64))
+    return out
+
+
+def oracle_ring_sampled(q, k, v, cp, rows_by_head, mode, causal=False, layout=0, scale=None, c_full=None):
+    """Oracle ring output for sampled rows, head by head (only the needed
+    K/V head is copied to the host).  Returns {(b,h): (o, lse, overshoot)}."""
+    Hq, Hkv = q.shape[1], k.shape[1]
+    G = Hq // Hkv
+    res = {}
+    kcache = {}
+    for (b, h), rows in rows_by_head.items():
+        key = (b, h // G)
+        if key not in kcache:
+            kcache.clear()
+            kcache[key] = (np32(k[b:b + 1, h // G:h // G + 1]), np32(v[b:b + 1, h // G:h // G + 1]))
+        kk, vv = kcache[key]
+        qq = np32(q[b:b + 1, h:h + 1])
+        cc = None
+        if mode == oracle.MODE_CONST_MAX:
+            cc, _ = oracle.const_max_bound(qq, kk, scale)  # one key max for the whole head
+        o, lse, ov = oracle.ring(qq, kk, vv, cp, mode=mode, causal=causal, layout=layout, rows=rows,
+                                 scale=scale, c=cc)
+        res[(b, h)] = (o, lse, ov)
+    return res

@@ -1,0 +1,120 @@
+"""The C ABI without a GPU: the library builds, loads and exports every entry
+point declared in include/ctxattn.h, and host-side validation returns the
+documented status codes before anything touches a device."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+FAKE = 4096  # an aligned, never-dereferenced pointer value: validation fails first
+
+
+@pytest.fixture(scope="module")
+def ca():
+    import context_attention_gb300 as m
+
+    m.build()
+    return m
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "ctxattn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ca_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(ca):
+    import ctypes
+
+    names = declared_functions()
+    assert len(names) >= 20
+    lib = ctypes.CDLL(ca.library_path())
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(ca):
+    lib = ca._load()
+    for code, name in ca.STATUS.items():
+        assert lib.ca_status_string(code).decode() == name
+    assert lib.ca_version() >= 100
+
+
+def ring(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, dtype=1, B=1, Hq=4, Hkv=2, S=1024, D=128, cp=4,
+             mode=0, causal=0, layout=0, scale=0.0, ws=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return lib.ca_ring_attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["dtype"], a["B"], a["Hq"],
+                                a["Hkv"], a["S"], a["D"], a["cp"], a["mode"], a["causal"], a["layout"],
+                                a["scale"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+def test_ring_validation_codes(ca):
+    lib = ca._load()
+    S = ca.STATUS
+    assert S[ring(lib, q=None)] == "CA_ERR_INVALID_ARG"
+    assert S[ring(lib, mode=7)] == "CA_ERR_INVALID_ARG"
+    assert S[ring(lib, layout=2)] == "CA_ERR_INVALID_ARG"
+    assert S[ring(lib, cp=0)] == "CA_ERR_INVALID_ARG"
+    assert S[ring(lib, dtype=5)] == "CA_ERR_INVALID_ARG"
+    assert S[ring(lib, S=3645, cp=8)] == "CA_ERR_SHAPE"
+    assert S[ring(lib, Hq=6, Hkv=4)] == "CA_ERR_SHAPE"
+    assert S[ring(lib, D=64)] == "CA_ERR_UNSUPPORTED"           # bf16 needs D = 128
+    assert S[ring(lib, dtype=0, D=160)] == "CA_ERR_UNSUPPORTED"  # fp32 needs D <= 128
+    assert S[ring(lib, q=FAKE + 2)] == "CA_ERR_ALIGNMENT"
+    assert S[ring(lib, mode=1)] == "CA_ERR_WORKSPACE"            # const max needs the bound buffer
+    need = lib.ca_ring_attn_fwd_workspace_size(1, 4, 2, 1024, 128, 4, 1)
+    assert need >= 4 * 4 * 1024
+    assert S[ring(lib, mode=1, ws=FAKE, ws_bytes=need - 1)] == "CA_ERR_WORKSPACE"
+    assert lib.ca_ring_attn_fwd_workspace_size(1, 4, 2, 1024, 128, 4, 0) == 0
+
+
+def test_partial_step_validation_codes(ca):
+    lib = ca._load()
+    S = ca.STATUS
+
+    def step(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=1, B=1, Hq=2, Hkv=2, Ls=256, D=128, qr=0, kr=0, cp=2, mode=0,
+                 causal=0, layout=0, scale=0.0, c=None, o=FAKE, lse=FAKE, stream=None)
+        a.update(kw)
+        return lib.ca_attn_partial_step(a["q"], a["k"], a["v"], a["dtype"], a["B"], a["Hq"], a["Hkv"], a["Ls"],
+                                        a["D"], a["qr"], a["kr"], a["cp"], a["mode"], a["causal"], a["layout"],
+                                        a["scale"], a["c"], a["o"], a["lse"], a["stream"])
+
+    assert S[step(qr=2)] == "CA_ERR_INVALID_ARG"
+    assert S[step(kr=-1)] == "CA_ERR_INVALID_ARG"
+    assert S[step(mode=1)] == "CA_ERR_INVALID_ARG"      # const max needs c
+    assert S[step(c=FAKE)] == "CA_ERR_INVALID_ARG"      # online max takes no c
+    assert S[step(lse=None)] == "CA_ERR_INVALID_ARG"
+    assert S[step(o=FAKE + 8)] == "CA_ERR_ALIGNMENT"
+
+
+def test_merge_bound_decode_layout_validation(ca):
+    lib = ca._load()
+    S = ca.STATUS
+    assert S[lib.ca_lse_merge(FAKE, FAKE, 0, 16, 128, None, FAKE, 0, None, None)] == "CA_ERR_INVALID_ARG"
+    assert S[lib.ca_lse_merge(FAKE, FAKE, 2, 16, 126, None, FAKE, 0, None, None)] == "CA_ERR_UNSUPPORTED"
+    assert S[lib.ca_const_max_bound(FAKE, FAKE, 1, 1, 6, 4, 64, 128, 0.0, FAKE, FAKE, None)] == "CA_ERR_SHAPE"
+    assert S[lib.ca_const_max_bound(FAKE, FAKE, 1, 1, 4, 4, 64, 128, 0.0, FAKE, None, None)] == "CA_ERR_INVALID_ARG"
+
+    def dec(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=1, N=2, Hq=8, Hkv=2, Lloc=256, D=128, W=4, I=16, seq=None,
+                 scale=0.0, o=FAKE, lse=FAKE, ws=FAKE, ws_bytes=1 << 30, stream=None)
+        a.update(kw)
+        return lib.ca_dcp_decode(a["q"], a["k"], a["v"], a["dtype"], a["N"], a["Hq"], a["Hkv"], a["Lloc"], a["D"],
+                                 a["W"], a["I"], a["seq"], a["scale"], a["o"], a["lse"], a["ws"], a["ws_bytes"],
+                                 a["stream"])
+
+    assert S[dec(Lloc=250)] == "CA_ERR_SHAPE"           # Lloc % interleave
+    assert S[dec(Hq=6, Hkv=4)] == "CA_ERR_SHAPE"
+    assert S[dec(dtype=0)] == "CA_ERR_UNSUPPORTED"
+    assert S[dec(Hq=32, Hkv=2)] == "CA_ERR_UNSUPPORTED"  # more than 8 query heads per KV head
+    assert S[dec(ws=None)] == "CA_ERR_WORKSPACE"
+    assert S[dec(ws_bytes=16)] == "CA_ERR_WORKSPACE"
+    assert lib.ca_dcp_decode_workspace_size(64, 32, 8, 32768, 128, 4, 16) > 64 * 32 * 128 * 4 * 4
+
+    assert S[lib.ca_layout_to_shards(FAKE, FAKE, 2, 100, 256, 8, 0, None)] == "CA_ERR_SHAPE"
+    assert S[lib.ca_layout_to_shards(FAKE, FAKE, 2, 64, 100, 8, 0, None)] == "CA_ERR_UNSUPPORTED"
+    assert S[lib.ca_dcp_shard_kv(FAKE, FAKE, 2, 100, 256, 4, 16, None)] == "CA_ERR_SHAPE"

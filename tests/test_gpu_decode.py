@@ -1,0 +1,103 @@
+"""GPU parity of DCP decode against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, np32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ca(cuda_device):
+    import context_attention_gb300 as m
+
+    m.build()
+    yield m
+    assert m.device_status() == 0, "a bounded device wait gave up"
+
+
+def run_case(ca, N, Hq, Hkv, W, I, Lloc, seq_lens, seed, scale=None):
+    from context_attention_gb300 import synth
+
+    q, k, v = synth.decode_inputs(N, Hq, Hkv, 128, W, Lloc, seed, device="cuda")
+    sl = None if seq_lens is None else torch.tensor(seq_lens, dtype=torch.int32, device="cuda")
+    o, lse = ca.dcp_decode(q, k, v, I, seq_lens=sl, softmax_scale=scale)
+    ro, rl = oracle.dcp_decode(np32(q), np32(k), np32(v), I, seq_lens=seq_lens, scale=scale)
+    assert_close(np32(o), ro, np32(lse), rl, what=f"decode N={N} Hq={Hq} Hkv={Hkv} W={W} Lloc={Lloc}")
+
+
+def test_decode_full_lengths(ca):
+    run_case(ca, N=3, Hq=8, Hkv=2, W=4, I=16, Lloc=512, seq_lens=None, seed=1)
+
+
+def test_decode_variable_lengths(ca):
+    """Lengths on and off block and virtual-block boundaries: 1 token (only
+    rank 0 holds anything), 17, 63, 64, 65, 1000, a full cache; the active
+    token is counted exactly once (owner only)."""
+    W, I, Lloc = 4, 16, 1024
+    lens = [1, 17, 63, 64, 65, 1000, W * Lloc, 2049]
+    run_case(ca, N=len(lens), Hq=4, Hkv=1, W=W, I=I, Lloc=Lloc, seq_lens=lens, seed=2)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (4, 1), (32, 8), (16, 2)])
+def test_decode_gqa_groups(ca, Hq, Hkv):
+    run_case(ca, N=2, Hq=Hq, Hkv=Hkv, W=2, I=16, Lloc=640, seq_lens=[1280, 700], seed=3)
+
+
+def test_decode_multi_split_and_garbage_tail(ca):
+    """Lloc spans several 4096-token splits; slots past each rank's valid
+    count hold NaN and must not leak into the result."""
+    from context_attention_gb300 import synth
+
+    N, Hq, Hkv, W, I, Lloc = 2, 8, 2, 4, 16, 9000 - 9000 % 16
+    q, k, v = synth.decode_inputs(N, Hq, Hkv, 128, W, Lloc, 4, device="cuda")
+    lens = [W * Lloc - 100, 20000]
+    for r in range(W):
+        for n in range(N):
+            lf = ca.dcp_local_filled(lens[n], W, I, I, r)
+            k[r, n, :, lf:] = float("nan")
+            v[r, n, :, lf:] = float("nan")
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    o, lse = ca.dcp_decode(q, k, v, I, seq_lens=sl)
+    kk, vv = torch.nan_to_num(k), torch.nan_to_num(v)
+    ro, rl = oracle.dcp_decode(np32(q), np32(kk), np32(vv), I, seq_lens=lens)
+    assert_close(np32(o), ro, np32(lse), rl, what="decode nan tail")
+
+
+def test_decode_zero_length_sequence(ca):
+    """seq_len = 0: every partial is empty: o = 0, lse = -inf."""
+    from context_attention_gb300 import synth
+
+    q, k, v = synth.decode_inputs(2, 4, 1, 128, 2, 256, 5, device="cuda")
+    sl = torch.tensor([0, 300], dtype=torch.int32, device="cuda")
+    o, lse = ca.dcp_decode(q, k, v, 16, seq_lens=sl)
+    assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    ro, rl = oracle.dcp_decode(np32(q[1:]), np32(k[:, 1:]), np32(v[:, 1:]), 16, seq_lens=[300])
+    assert_close(np32(o[1:]), ro, np32(lse[1:]), rl, what="decode second seq")
+
+
+def test_decode_matches_global_attention(ca):
+    """Shard a global KV cache with the library's interleave kernel, decode,
+    and compare with plain attention of the query over the global prefix
+    (the oracle's full attention)."""
+    from context_attention_gb300 import synth
+
+    N, Hq, Hkv, W, I, L = 2, 4, 2, 4, 16, 1024
+    g = torch.Generator(device="cuda")
+    g.manual_seed(6)
+    q = torch.randn(N, Hq, 128, generator=g, device="cuda").to(torch.bfloat16)
+    kg = torch.randn(N, Hkv, L, 128, generator=g, device="cuda").to(torch.bfloat16)
+    vg = torch.randn(N, Hkv, L, 128, generator=g, device="cuda").to(torch.bfloat16)
+    ks, vs = ca.dcp_shard_kv(kg, W, I), ca.dcp_shard_kv(vg, W, I)
+    lens = [L, 555]
+    o, lse = ca.dcp_decode(q, ks, vs, I, seq_lens=torch.tensor(lens, dtype=torch.int32, device="cuda"))
+    for n in range(N):
+        Ln = lens[n]
+        qf = np.zeros((1, Hq, Ln, 128), np.float32)
+        qf[0, :, 0] = np32(q[n])
+        ro, rl = oracle.attention(qf, np32(kg[n:n + 1, :, :Ln]), np32(vg[n:n + 1, :, :Ln]),
+                                  rows=[h * Ln for h in range(Hq)])
+        assert_close(np32(o[n]), ro, np32(lse[n]), rl, what=f"decode vs global n={n}")
+    del synth

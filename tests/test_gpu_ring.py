@@ -1,0 +1,233 @@
+"""GPU parity of ring attention (fused ring, one ring step, LSE merge, bound)
+against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, np32
+
+pytestmark = pytest.mark.gpu
+
+MODES = {"online_max": oracle.MODE_ONLINE_MAX, "const_max": oracle.MODE_CONST_MAX}
+LAYOUTS = {"contiguous": oracle.LAYOUT_CONTIGUOUS, "striped": oracle.LAYOUT_STRIPED}
+
+
+@pytest.fixture(scope="module")
+def ca(cuda_device):
+    import context_attention_gb300 as m
+
+    m.build()
+    yield m
+    assert m.device_status() == 0, "a bounded device wait gave up"
+
+
+def gen(B, Hq, Hkv, S, D, seed, dtype):
+    from context_attention_gb300 import synth
+
+    return synth.normal_qkv(B, Hq, Hkv, S, D, seed, dtype=dtype, device="cuda")
+
+
+def oracle_ring(q, k, v, cp, mode, causal, layout, scale=None):
+    o, lse, _ = oracle.ring(np32(q), np32(k), np32(v), cp, mode=MODES[mode], causal=causal,
+                            layout=LAYOUTS[layout], scale=scale)
+    return o, lse
+
+
+# --------------------------------------------------------------- fp32 (SIMT)
+
+
+@pytest.mark.parametrize("mode", ["online_max", "const_max"])
+def test_fp32_tiny_config(ca, mode):
+    """fp32, B=1, H=2, S=256, D=64, cp=2: within 1e-4 of the oracle."""
+    q, k, v = gen(1, 2, 2, 256, 64, 1, torch.float32)
+    o, lse = ca.ring_attn_fwd(q, k, v, 2, mode=mode)
+    ro, rl = oracle_ring(q, k, v, 2, mode, False, "contiguous")
+    assert_close(np32(o), ro, np32(lse), rl, dtype=torch.float32, what=f"fp32 {mode}")
+
+
+@pytest.mark.parametrize("mode", ["online_max", "const_max"])
+@pytest.mark.parametrize("causal,layout", [(False, "contiguous"), (True, "contiguous"), (True, "striped")])
+def test_fp32_gqa_ragged_causal(ca, mode, causal, layout):
+    # Ls = 70 (not a multiple of the 16-row block or the 32-key tile), GQA 4:2, D = 40
+    q, k, v = gen(2, 4, 2, 210, 40, 2, torch.float32)
+    o, lse = ca.ring_attn_fwd(q, k, v, 3, mode=mode, causal=causal, layout=layout, softmax_scale=0.3)
+    ro, rl = oracle_ring(q, k, v, 3, mode, causal, layout, scale=0.3)
+    assert_close(np32(o), ro, np32(lse), rl, dtype=torch.float32, what=f"fp32 {mode} {layout}")
+
+
+# --------------------------------------------------------------- bf16 (tcgen05)
+
+
+@pytest.mark.parametrize("mode", ["online_max", "const_max"])
+@pytest.mark.parametrize("causal,layout", [(False, "contiguous"), (True, "contiguous"), (True, "striped")])
+def test_bf16_small(ca, mode, causal, layout):
+    """bf16, D=128, B=1, H=2, S=1024, cp=4 (Ls=256: two query tiles per unit)."""
+    q, k, v = gen(1, 2, 2, 1024, 128, 3, torch.bfloat16)
+    o, lse = ca.ring_attn_fwd(q, k, v, 4, mode=mode, causal=causal, layout=layout)
+    ro, rl = oracle_ring(q, k, v, 4, mode, causal, layout)
+    assert_close(np32(o), ro, np32(lse), rl, what=f"bf16 {mode} causal={causal} {layout}")
+
+
+@pytest.mark.parametrize("mode", ["online_max", "const_max"])
+@pytest.mark.parametrize("causal,layout", [(False, "contiguous"), (True, "contiguous"), (True, "striped")])
+def test_bf16_gqa_ragged(ca, mode, causal, layout):
+    """GQA 4:2 (kv head h//2), Ls = 300 (ragged: 3 key tiles, last one partial;
+    the second query tile of the last unit mostly empty), cp = 3, B = 2."""
+    q, k, v = gen(2, 4, 2, 900, 128, 4, torch.bfloat16)
+    o, lse = ca.ring_attn_fwd(q, k, v, 3, mode=mode, causal=causal, layout=layout)
+    ro, rl = oracle_ring(q, k, v, 3, mode, causal, layout)
+    assert_close(np32(o), ro, np32(lse), rl, what=f"bf16 gqa {mode} causal={causal} {layout}")
+
+
+@pytest.mark.parametrize("S,cp", [(128, 1), (8, 8), (136, 8), (1, 1)])
+def test_bf16_degenerate_shapes(ca, S, cp):
+    """cp = 1 (plain attention), Ls = 1 (one token per shard), Ls = 17, S = 1."""
+    q, k, v = gen(1, 2, 1, S, 128, 5, torch.bfloat16)
+    for mode in ("online_max", "const_max"):
+        for causal, layout in ((False, "contiguous"), (True, "striped"), (True, "contiguous")):
+            o, lse = ca.ring_attn_fwd(q, k, v, cp, mode=mode, causal=causal, layout=layout)
+            ro, rl = oracle_ring(q, k, v, cp, mode, causal, layout)
+            assert_close(np32(o), ro, np32(lse), rl, what=f"S={S} cp={cp} {mode} {layout}")
+
+
+def test_bf16_dit_const_max(ca):
+    """Cross-head RMS-normalised q/k (the DiT recipe), H=8, S=2048, cp=8,
+    const max and online max against the oracle."""
+    from context_attention_gb300 import synth
+
+    q, k, v = synth.dit_qk(1, 8, 2048, 128, seed=6, device="cuda")
+    for mode in ("const_max", "online_max"):
+        o, lse = ca.ring_attn_fwd(q, k, v, 8, mode=mode)
+        ro, rl = oracle_ring(q, k, v, 8, mode, False, "contiguous")
+        assert_close(np32(o), ro, np32(lse), rl, what=f"dit {mode}")
+
+
+def test_bf16_error_distribution_vs_oracle_rounding(ca):
+    """The GPU's error against exact attention is of the same order as the
+    error of exact attention computed from bf16-rounded outputs (the const-max
+    page's validation advice: compare error distributions)."""
+    q, k, v = gen(1, 2, 2, 1024, 128, 7, torch.bfloat16)
+    o, _ = ca.ring_attn_fwd(q, k, v, 4, mode="const_max")
+    ro, _ = oracle_ring(q, k, v, 4, "const_max", False, "contiguous")
+    gpu_err = np.abs(np32(o).reshape(ro.shape) - ro)
+    round_err = np.abs(torch.tensor(ro).to(torch.bfloat16).double().numpy() - ro)
+    assert gpu_err.mean() <= 4 * round_err.mean() + 1e-5
+
+
+# --------------------------------------------------------------- steps + merge
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("causal,layout", [(False, "contiguous"), (True, "contiguous"), (True, "striped")])
+def test_partial_steps_merge_to_ring(ca, dtype, causal, layout):
+    """Every ring step through ca_attn_partial_step, merged with ca_lse_merge
+    (online: LSE weights; const max: pure addition with the bound), equals the
+    oracle's ring; each step's partial equals the oracle's shard partial."""
+    cp, Ls = 4, 160
+    D = 128 if dtype == torch.bfloat16 else 64
+    q, k, v = gen(1, 4, 2, cp * Ls, D, 8, dtype)
+    tol_dtype = dtype
+    for mode in ("online_max", "const_max"):
+        c_full = None
+        if mode == "const_max":
+            c_full, _ = ca.const_max_bound(q, k)
+        ro, rl = oracle_ring(q, k, v, cp, mode, causal, layout)
+        ro = ro.reshape(1, 4, cp * Ls, D)
+        rl = rl.reshape(1, 4, cp * Ls)
+        for r in range(cp):
+            qs = q[:, :, r * Ls:(r + 1) * Ls].contiguous()
+            o_parts, l_parts = [], []
+            for t in range(cp):
+                s = ca.ring_kv_shard(r, t, cp)
+                ks = k[:, :, s * Ls:(s + 1) * Ls].contiguous()
+                vs = v[:, :, s * Ls:(s + 1) * Ls].contiguous()
+                cs = None if c_full is None else c_full[:, :, r * Ls:(r + 1) * Ls].contiguous()
+                op, lp = ca.attn_partial_step(qs, ks, vs, r, s, cp, mode=mode, causal=causal, layout=layout, c=cs)
+                if mode == "online_max":
+                    rows = np.array([(hh * cp * Ls + r * Ls + a) for hh in range(4) for a in range(Ls)])
+                    so, sl = oracle.shard_partial(np32(q), np32(k), np32(v), s, cp, causal=causal,
+                                                  layout=LAYOUTS[layout], rows=rows)
+                    assert_close(np32(op), so, np32(lp), sl, dtype=tol_dtype, what=f"step r={r} s={s}")
+                o_parts.append(op)
+                l_parts.append(lp)
+            cm = None if c_full is None else c_full[:, :, r * Ls:(r + 1) * Ls].contiguous()
+            o, lse = ca.lse_merge(torch.stack(o_parts), torch.stack(l_parts), c=cm, out_dtype=torch.float32)
+            assert_close(np32(o), ro[:, :, r * Ls:(r + 1) * Ls], np32(lse), rl[:, :, r * Ls:(r + 1) * Ls],
+                         dtype=tol_dtype, what=f"merged {mode} r={r}")
+
+
+def test_partial_step_fully_masked(ca):
+    """Contiguous causal, queries of shard 0 against keys of shard 2: nothing
+    is visible, so o = 0 and lse = -inf (both dtypes)."""
+    for dtype, D in ((torch.bfloat16, 128), (torch.float32, 32)):
+        q, k, v = gen(1, 2, 2, 128, D, 9, dtype)
+        o, lse = ca.attn_partial_step(q, k, v, 0, 2, 4, causal=True, layout="contiguous")
+        assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_lse_merge_kernel(ca):
+    rng = np.random.default_rng(10)
+    n, R, D = 5, 300, 128
+    op = rng.standard_normal((n, R, D)).astype(np.float32)
+    lp = (rng.standard_normal((n, R)) * 3).astype(np.float32)
+    lp[1, ::7] = -np.inf
+    lp[:, 5] = -np.inf  # an all-empty row
+    ro, rl = oracle.lse_merge(op, lp)
+    for out_dtype in (torch.float32, torch.bfloat16):
+        o, lse = ca.lse_merge(torch.tensor(op, device="cuda"), torch.tensor(lp, device="cuda"), out_dtype=out_dtype)
+        assert_close(np32(o), ro, np32(lse), rl, dtype=torch.float32 if out_dtype == torch.float32 else torch.bfloat16,
+                     what=f"merge {out_dtype}")
+
+
+def test_const_max_bound_kernel(ca):
+    from context_attention_gb300 import synth
+
+    for dtype, D in ((torch.bfloat16, 128), (torch.float32, 64), (torch.float32, 20)):
+        q, k, _ = synth.normal_qkv(2, 4, 2, 700, D, 11, dtype=dtype, device="cuda")
+        c, kmax2 = ca.const_max_bound(q, k, softmax_scale=0.2)
+        rc, rk = oracle.const_max_bound(np32(q), np32(k), scale=0.2)
+        np.testing.assert_allclose(np32(kmax2), rk, rtol=2e-6)
+        np.testing.assert_allclose(np32(c), rc, rtol=2e-6)
+
+
+# --------------------------------------------------------------- layouts (bit-exact)
+
+
+def test_layout_permutations_bit_exact(ca):
+    x = torch.randint(-2**15, 2**15, (2, 3, 96, 64), dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    for cp in (1, 4, 8):
+        Ls = 96 // cp
+        for layout in ("contiguous", "striped"):
+            y = ca.layout_to_shards(x, cp, layout)
+            rows = [ca.layout_global_index(layout, cp, Ls, r) for r in range(96)]
+            assert torch.equal(y.view(torch.int16), x[:, :, rows].view(torch.int16))
+            assert torch.equal(ca.layout_from_shards(y, cp, layout).view(torch.int16), x.view(torch.int16))
+
+
+def test_dcp_shard_kv_bit_exact(ca):
+    W, I, L = 4, 16, 256
+    kv = torch.randint(-2**15, 2**15, (3, 2, L, 128), dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    sh = ca.dcp_shard_kv(kv, W, I)
+    own, loc = oracle.dcp_deal(L, W, I)
+    ref = np.zeros((W, 3, 2, L // W, 128), np.int16)
+    kvn = kv.view(torch.int16).cpu().numpy()
+    for p in range(L):
+        ref[own[p], :, :, loc[p]] = kvn[:, :, p]
+    assert np.array_equal(sh.view(torch.int16).cpu().numpy(), ref)
+
+
+def test_striped_ring_equals_contiguous_after_unpermuting(ca):
+    """Invariant (e) on the GPU path: causal ring attention over striped
+    storage, un-permuted, equals the contiguous causal result of the global
+    sequence (both from the CUDA kernels), and both match the oracle."""
+    cp, S = 4, 1024
+    qg, kg, vg = gen(1, 2, 2, S, 128, 12, torch.bfloat16)
+    oc, lc = ca.ring_attn_fwd(qg, kg, vg, cp, causal=True, layout="contiguous")
+    qs, ks, vs = (ca.layout_to_shards(t, cp, "striped") for t in (qg, kg, vg))
+    os_, ls_ = ca.ring_attn_fwd(qs, ks, vs, cp, causal=True, layout="striped")
+    back = ca.layout_from_shards(os_, cp, "striped")
+    lback = ca.layout_from_shards(ls_.unsqueeze(-1).repeat(1, 1, 1, 4).contiguous(), cp, "striped")[..., 0]
+    d = (back.float() - oc.float()).abs()
+    assert d.max().item() <= 2e-2 and d.mean().item() <= 2e-3
+    assert (lback - lc).abs().max().item() <= 1e-3
