@@ -246,7 +246,7 @@ def bench_prefill(ca, torch, steps, warmup, pg, dev_index):
     return res
 
 
-def bench_decode(ca, torch, steps, warmup, pg):
+def bench_decode(ca, torch, steps, warmup, pg, dev_index):
     from context_attention_gb300 import synth
 
     c = DECODE
@@ -263,46 +263,85 @@ def bench_decode(ca, torch, steps, warmup, pg):
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        ca.dcp_decode(q, k, v, c["I"], out=o, lse=lse, workspace=ws)
-    b.record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        a.record(stream)
+        for _ in range(steps):
+            ca.dcp_decode(q, k, v, c["I"], out=o, lse=lse, workspace=ws)
+        b.record(stream)
+        torch.cuda.synchronize()
     barrier(pg)
     ms = a.elapsed_time(b) / steps
     assert ca.device_status() == 0
     del q, k, v
     torch.cuda.empty_cache()
-    return dict(ms=ms)
+    return dict(ms=ms, clocks=clk.summary())
 
 
-def cpu_baseline_prefill(torch, seconds=15.0):
-    """The oracle as it stands, on a bounded sample of DiT-workload rows."""
-    import numpy as np
+class OracleSampler:
+    """The fp64 oracle as it stands, on bounded samples of DiT-workload rows
+    (inputs drawn once on the host with the same recipe and seed)."""
 
-    import oracle
-    from context_attention_gb300 import synth
+    def __init__(self, heads=8):
+        import numpy as np
 
-    c = PREFILL
-    # one head of the same workload, generated on the host
-    q, k, v = synth.dit_qk(1, c["H"], c["S"], c["D"], seed=c["seed"], device="cpu")
-    qq, kk, vv = (t[:, :1].float().numpy() for t in (q, k, v))
-    bound, _ = oracle.const_max_bound(qq, kk)
-    rng = np.random.default_rng(0)
+        import oracle
+        from context_attention_gb300 import synth
 
-    def run(n):
-        rows = np.sort(rng.choice(c["S"], size=n, replace=False))
+        c = PREFILL
+        self.oracle, self.np, self.heads = oracle, np, heads
+        q, k, v = synth.dit_qk(1, c["H"], c["S"], c["D"], seed=c["seed"], device="cpu")
+        self.q, self.k, self.v = (t[:, :heads].float().numpy() for t in (q, k, v))
+        self.bound, _ = oracle.const_max_bound(self.q, self.k)
+        self.rng = np.random.default_rng(0)
+
+    def run(self, n):
+        c = PREFILL
+        rows = self.np.sort(self.rng.choice(self.heads * c["S"], size=n, replace=False))
         t0 = time.perf_counter()
-        oracle.ring(qq, kk, vv, c["cp"], mode=oracle.MODE_CONST_MAX, rows=rows, c=bound)
+        self.oracle.ring(self.q, self.k, self.v, c["cp"], mode=self.oracle.MODE_CONST_MAX, rows=rows, c=self.bound)
         return time.perf_counter() - t0
 
-    t_probe = run(64)
-    n = int(min(c["S"], max(64, 64 * seconds / max(t_probe, 1e-6))))
-    t = run(n)
-    flops = 4.0 * c["S"] * c["D"] * n
-    return dict(value=flops / t / 1e12, unit="TFLOP/s", cores=oracle.num_threads(),
-                kind="oracle", sample=f"{n} query rows of head 0 of the DiT workload (const max), {t:.1f} s",
-                seconds=t)
+    def rows_for(self, seconds):
+        t = self.run(128)
+        return int(min(self.heads * PREFILL["S"], max(64, 128 * seconds / max(t, 1e-6))))
+
+    def measure(self, n):
+        t = self.run(n)
+        flops = 4.0 * PREFILL["S"] * PREFILL["D"] * n
+        threads = self.oracle.num_threads()
+        return dict(value=flops / t / 1e12, unit="TFLOP/s", cores=threads, kind="oracle",
+                    sample=f"{n} query rows of heads 0-{self.heads - 1} of the DiT workload (const max), "
+                    f"{t:.1f} s on {threads} threads", seconds=t)
+
+
+def cpu_baseline_prefill(seconds=15.0):
+    smp = OracleSampler()
+    return smp.measure(smp.rows_for(seconds))
+
+
+def run_profile_case(args):
+    """One small launch of one kernel, for ncu captures (inputs > L2, a few GB)."""
+    import torch
+
+    import context_attention_gb300 as ca
+    from context_attention_gb300 import synth
+
+    torch.cuda.set_device(0)
+    if args.profile == "ring":
+        # DiT recipe with 16 heads: q,k,v 201 MB (> L2), one launch ~2 ms
+        q, k, v = synth.dit_qk(1, 16, PREFILL["S"], PREFILL["D"], seed=PREFILL["seed"], device="cuda")
+        c, _ = ca.const_max_bound(q, k)
+        for _ in range(args.warmup + 1):
+            ca.ring_attn_fwd_bounded(q, k, v, c, PREFILL["cp"])
+    else:
+        # decode recipe with 8 sequences: K+V 4.3 GB, one launch ~0.6 ms
+        d = DECODE
+        q, kd, vd = synth.decode_inputs(8, d["Hq"], d["Hkv"], d["D"], d["W"], d["Lloc"], d["seed"], device="cuda")
+        for _ in range(args.warmup + 1):
+            ca.dcp_decode(q, kd, vd, d["I"])
+    torch.cuda.synchronize()
+    assert ca.device_status() == 0
+    print(f"profile case {args.profile} done")
 
 
 def run_ours(args):
@@ -315,7 +354,7 @@ def run_ours(args):
     ca._load()
     peaks, peak_src = load_peaks()
     pre = bench_prefill(ca, torch, args.steps, args.warmup, pg, local)
-    dec = None if args.skip_decode else bench_decode(ca, torch, args.steps, args.warmup, pg)
+    dec = None if args.skip_decode else bench_decode(ca, torch, args.steps, args.warmup, pg, local)
 
     total_ms = max_over_ranks(pre["total_ms"], pg)
     ms_per_step = total_ms / args.steps
@@ -345,7 +384,10 @@ def run_ours(args):
         "roofline": {"kernel": "ring_tc_kernel", "bound": "tensor", "achieved": round(ring_tflops, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(ring_tflops / peak, 4),
                      "traffic": read_traffic("ring_tc_kernel_dit16k.txt"),
-                     "peak_source": f"{peak_src} {'sustained' if long_run else 'burst'} bf16",
+                     "peak_source": f"{peak_src} {'sustained' if long_run else 'burst'} bf16 "
+                                    f"(timed region {total_ms / 1e3:.2f} s)",
+                     "frac_of_burst": round(ring_tflops / peaks["bf16_tflops"], 4),
+                     "frac_of_sustained": round(ring_tflops / peaks["bf16_tflops_sustained"], 4),
                      "bound_pass_ms": round(pre["bound_ms"], 4), "ring_ms": round(pre["ring_ms"], 4)},
         "clocks": pre["clocks"],
         "e2e": {"value": round(flops / (pre["e2e_ms"] / 1e3) / 1e12 * world, 2), "unit": "TFLOP/s",
@@ -363,9 +405,10 @@ def run_ours(args):
                                       "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                       "frac": round(gbs / peaks["hbm_gbs"], 4),
                                       "traffic": read_traffic("dcp_decode_kernel_131k.txt"),
-                                      "peak_source": f"{peak_src} copy bandwidth"}}
+                                      "peak_source": f"{peak_src} copy bandwidth"},
+                         "clocks": dec["clocks"]}
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline_prefill(torch, seconds=args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline_prefill(seconds=args.cpu_seconds)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if pg is not None:
@@ -379,19 +422,17 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import torch
-
-    import oracle
-
-    per_step = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    smp = OracleSampler()
+    # each step: a bounded sample sized so the whole run stays within ~2 minutes
+    per_step = max(0.1, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    n = smp.rows_for(per_step)
     for _ in range(args.warmup):
-        cpu_baseline_prefill(torch, seconds=per_step / 4)
-    vals, secs, samples = [], [], []
+        smp.run(n)
+    vals, secs, last = [], [], None
     for _ in range(args.steps):
-        r = cpu_baseline_prefill(torch, seconds=per_step)
-        vals.append(r["value"])
-        secs.append(r["seconds"])
-        samples.append(r["sample"])
+        last = smp.measure(n)
+        vals.append(last["value"])
+        secs.append(last["seconds"])
     value = statistics.mean(vals)
     out = {
         "impl": "reference",
@@ -410,8 +451,8 @@ def run_reference(args):
         "config": {"workload": "DiT const-max ring self-attention prefill", "B": PREFILL["B"], "H": PREFILL["H"],
                    "S": PREFILL["S"], "D": PREFILL["D"], "cp_size": PREFILL["cp"], "mode": "const_max",
                    "layout": "contiguous", "causal": False, "parallelism": "host cores"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": samples[-1]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": f"each step: {last['sample']}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
@@ -420,16 +461,20 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile", choices=["ring", "decode"], default=None,
+                    help="run one small launch of one kernel (for ncu captures) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.profile:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
