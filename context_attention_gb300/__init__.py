@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "CtxAttnError", "build", "library_path", "ring_attn_fwd", "ring_attn_fwd_bounded", "attn_partial_step", "lse_merge",
-    "const_max_bound", "dcp_decode", "layout_to_shards", "layout_from_shards", "dcp_shard_kv",
+    "const_max_bound", "dcp_decode", "dcp_decode_noalloc", "layout_to_shards", "layout_from_shards", "dcp_shard_kv",
     "layout_global_index", "layout_shard_row", "ring_kv_shard", "dcp_owner", "dcp_local_index",
     "dcp_local_to_global", "dcp_local_filled", "dcp_active_mask", "dcp_slot_mapping",
     "device_status", "ring_attn_fwd_workspace_size", "dcp_decode_workspace_size",
@@ -77,6 +77,7 @@ def _load():
             "ca_const_max_bound": ([P, P, I, I, I, I, I64, I, F, P, P, P], I),
             "ca_dcp_decode_workspace_size": ([I, I, I, I64, I, I, I], SZ),
             "ca_dcp_decode": ([P, P, P, I, I, I, I, I64, I, I, I, P, F, P, P, P, SZ, P], I),
+            "ca_dcp_decode_noalloc": ([P, P, P, I, I, I, I, I64, I, I, I, P, F, P, P, P], I),
             "ca_layout_to_shards": ([P, P, I64, I64, I64, I, I, P], I),
             "ca_layout_from_shards": ([P, P, I64, I64, I64, I, I, P], I),
             "ca_dcp_shard_kv": ([P, P, I64, I64, I64, I, I, P], I),
@@ -256,6 +257,33 @@ def dcp_decode(q, k_shards, v_shards, interleave, seq_lens=None, softmax_scale=N
                            D, W, interleave, _ptr(seq_lens), float(softmax_scale or 0.0), _ptr(out),
                            _ptr(lse), _ptr(workspace), workspace.numel(), _stream(q))
     _check("ca_dcp_decode", st)
+    return out, lse
+
+
+def dcp_decode_noalloc(q, k_shards, v_shards, interleave, seq_lens=None, softmax_scale=None, out=None,
+                       lse=None):
+    """DCP decode through the allocation-free entry point.
+
+    For callers that cannot allocate device memory at call time (their
+    framework's allocator owns all of it, or their enqueue path may not
+    allocate): the library keeps the split-KV partials in a built-in 16 MiB
+    scratch array instead of a workspace.  Pass ``out`` and ``lse`` to keep
+    this call free of allocations on the Python side too.  Larger problems
+    raise CtxAttnError (CA_ERR_WORKSPACE)."""
+    lib = _load()
+    _need(q, "q", 3)
+    _need(k_shards, "k_shards", 5)
+    _need(v_shards, "v_shards", 5)
+    N, Hq, D = q.shape
+    W, _, Hkv, Lloc, _ = k_shards.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(N, Hq, device=q.device, dtype=torch.float32)
+    st = lib.ca_dcp_decode_noalloc(_ptr(q), _ptr(k_shards), _ptr(v_shards), DTYPE[q.dtype], N, Hq, Hkv, Lloc,
+                                   D, W, interleave, _ptr(seq_lens), float(softmax_scale or 0.0), _ptr(out),
+                                   _ptr(lse), _stream(q))
+    _check("ca_dcp_decode_noalloc", st)
     return out, lse
 
 

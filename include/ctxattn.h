@@ -204,6 +204,31 @@ ca_status ca_dcp_decode(const void *q, const void *k_shards,
                         float *lse, void *workspace, size_t workspace_bytes,
                         void *stream);
 
+/* DCP decode without a workspace, for callers that cannot allocate device
+ * memory at call time: code running inside a framework whose allocator
+ * already owns all device memory, or plugin-style enqueue paths that must
+ * not allocate.  The pages have no counterpart of this call; it exists for
+ * such callers only.
+ *
+ * Same arguments, results and errors as ca_dcp_decode, minus the workspace.
+ * The split-KV partials live in a scratch array built into the library's
+ * device image: 16 MiB, held on every GPU that loads the library until the
+ * process exits.  A problem whose partials need more than that
+ * (ca_dcp_decode_workspace_size() > 16 MiB) is rejected with
+ * CA_ERR_WORKSPACE before anything is enqueued.  The call allocates nothing.
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress, once per device); make that first call before any
+ * stream capture.  All calls on a device share the one scratch array, so
+ * calls whose kernels overlap on the GPU race on it and must be serialised
+ * by the caller.  Nothing in it needs to start at zero: every partial the
+ * merge reads is written by the same call. */
+ca_status ca_dcp_decode_noalloc(const void *q, const void *k_shards,
+                                const void *v_shards, ca_dtype dtype, int N,
+                                int Hq, int Hkv, int64_t Lloc, int D, int dcp,
+                                int interleave, const int32_t *seq_lens,
+                                float softmax_scale, void *o, float *lse,
+                                void *stream);
+
 /* ------------------------------------------------------------------------
  * Device layout permutations (bit-exact copies of rows of row_bytes bytes).
  *
