@@ -334,9 +334,9 @@ def run_profile_case(args):
         for _ in range(args.warmup + 1):
             ca.ring_attn_fwd_bounded(q, k, v, c, PREFILL["cp"])
     else:
-        # decode recipe with 8 sequences: K+V 4.3 GB, one launch ~0.6 ms
+        # decode recipe with 4 sequences: K+V 2.1 GB (> L2), one launch ~0.3 ms
         d = DECODE
-        q, kd, vd = synth.decode_inputs(8, d["Hq"], d["Hkv"], d["D"], d["W"], d["Lloc"], d["seed"], device="cuda")
+        q, kd, vd = synth.decode_inputs(4, d["Hq"], d["Hkv"], d["D"], d["W"], d["Lloc"], d["seed"], device="cuda")
         for _ in range(args.warmup + 1):
             ca.dcp_decode(q, kd, vd, d["I"])
     torch.cuda.synchronize()

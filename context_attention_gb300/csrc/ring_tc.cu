@@ -183,6 +183,112 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int i, i
   }
 }
 
+// Orders every use of registers filled by tcgen05.ld after the wait::ld that
+// makes them valid (the compiler sees the wait as unrelated to them).
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 8)
+    asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]),
+                 "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+template <bool kMask>
+__device__ __forceinline__ float chunk_max(const uint32_t (&r)[32], int col0, int vis_max, float mx) {
+  if (kMask) {
+#pragma unroll
+    for (int x = 0; x < 32; ++x)
+      mx = fmaxf(mx, col0 + x > vis_max ? -INFINITY : __uint_as_float(r[x]));
+    return mx;
+  }
+  float a = mx, b = __uint_as_float(r[0]);
+#pragma unroll
+  for (int x = 1; x < 31; x += 2) {
+    a = max3(a, __uint_as_float(r[x]), __uint_as_float(r[x + 1]));
+  }
+  return max3(a, b, __uint_as_float(r[31]));
+}
+
+// Row maximum of the 128 raw scores of this thread's TMEM lane; loads are
+// software-pipelined so that one 32-column load is in flight while the
+// previous one is reduced.
+template <bool kMask>
+__device__ __forceinline__ float row_max_from_tmem(uint32_t tS, int vis_max) {
+  uint32_t ra[32], rb[32];
+  float mx = -INFINITY;
+  tmem_ld32(tS, ra);
+  tmem_ld_wait();
+  reg_fence(ra);
+  tmem_ld32(tS + 32, rb);
+  mx = chunk_max<kMask>(ra, 0, vis_max, mx);
+  tmem_ld_wait();
+  reg_fence(rb);
+  tmem_ld32(tS + 64, ra);
+  mx = chunk_max<kMask>(rb, 32, vis_max, mx);
+  tmem_ld_wait();
+  reg_fence(ra);
+  tmem_ld32(tS + 96, rb);
+  mx = chunk_max<kMask>(ra, 64, vis_max, mx);
+  tmem_ld_wait();
+  reg_fence(rb);
+  return chunk_max<kMask>(rb, 96, vis_max, mx);
+}
+
+// 32 scores -> 16 packed bf16 pairs of p = 2^(s*sl2 - ref), written to TMEM
+// columns [16*ch, 16*ch + 16) of the row; returns the chunk's sum of p.
+template <bool kMask>
+__device__ __forceinline__ float exp_chunk(const uint32_t (&r)[32], int ch, int vis_max, float sl2,
+                                           float ref, uint32_t tS) {
+  uint32_t pk[16];
+  float s_even = 0.f, s_odd = 0.f;
+#pragma unroll
+  for (int x = 0; x < 16; ++x) {
+    float s0 = __uint_as_float(r[2 * x]), s1 = __uint_as_float(r[2 * x + 1]);
+    if (kMask) {
+      if (ch * 32 + 2 * x > vis_max) s0 = -INFINITY;
+      if (ch * 32 + 2 * x + 1 > vis_max) s1 = -INFINITY;
+    }
+    const float p0 = ex2(fmaf(s0, sl2, -ref));
+    const float p1 = ex2(fmaf(s1, sl2, -ref));
+    s_even += p0;
+    s_odd += p1;
+    pk[x] = pack_bf16x2(p0, p1);
+  }
+  tmem_st16(tS + ch * 16, pk);
+  return s_even + s_odd;
+}
+
+// Pass 2 over one S row: exp, row sum, P (bf16) back into TMEM, with the
+// next 32-column load in flight while the current chunk is processed.  P
+// block ch overwrites S columns [16ch, 16ch+16), which were already read.
+template <bool kMask>
+__device__ __forceinline__ float exp_row_to_tmem(uint32_t tS, int vis_max, float sl2, float ref) {
+  uint32_t ra[32], rb[32];
+  float sum = 0.f;
+  tmem_ld32(tS, ra);
+  tmem_ld_wait();
+  reg_fence(ra);
+  tmem_ld32(tS + 32, rb);
+  sum += exp_chunk<kMask>(ra, 0, vis_max, sl2, ref, tS);
+  tmem_ld_wait();
+  reg_fence(rb);
+  tmem_ld32(tS + 64, ra);
+  sum += exp_chunk<kMask>(rb, 1, vis_max, sl2, ref, tS);
+  tmem_ld_wait();
+  reg_fence(ra);
+  tmem_ld32(tS + 96, rb);
+  sum += exp_chunk<kMask>(ra, 2, vis_max, sl2, ref, tS);
+  tmem_ld_wait();
+  reg_fence(rb);
+  sum += exp_chunk<kMask>(rb, 3, vis_max, sl2, ref, tS);
+  return sum;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const TcParams P) {
@@ -388,19 +494,9 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         if (const_max) {
           mref = c_log2;
         } else {
-          // pass 1: row maximum straight from TMEM, 32 columns at a time
-          float mx = -INFINITY;
-#pragma unroll
-          for (int ch = 0; ch < kBN / 32; ++ch) {
-            uint32_t r[32];
-            tmem_ld32(tS + ch * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) {
-              const float v = (need_mask && ch * 32 + x > vis_max) ? -INFINITY : __uint_as_float(r[x]);
-              mx = fmaxf(mx, v);
-            }
-          }
+          // pass 1: row maximum straight from TMEM; the next 32-column load is
+          // in flight while the current one is reduced
+          float mx = need_mask ? row_max_from_tmem<true>(tS, vis_max) : row_max_from_tmem<false>(tS, vis_max);
           mx *= P.scale_log2;
           float fac = 1.f;
           bool need_o = false;
@@ -417,6 +513,7 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
               uint32_t r[32];
               tmem_ld32(tO + ch * 32, r);
               tmem_ld_wait();
+              reg_fence(r);
 #pragma unroll
               for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * f);
               tmem_st32(tO + ch * 32, r);
@@ -427,27 +524,8 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         }
         // pass 2: p = 2^(s*scale*log2e - ref), row sum, bf16 P written over
         // the S columns already consumed (P column block ch < S block ch+1)
-        float psum = 0.f;
-#pragma unroll
-        for (int ch = 0; ch < kBN / 32; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(tS + ch * 32, r);
-          tmem_ld_wait();
-          uint32_t pk[16];
-#pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            float s0 = __uint_as_float(r[2 * x]), s1 = __uint_as_float(r[2 * x + 1]);
-            if (need_mask) {
-              if (ch * 32 + 2 * x > vis_max) s0 = -INFINITY;
-              if (ch * 32 + 2 * x + 1 > vis_max) s1 = -INFINITY;
-            }
-            const float p0 = ex2(fmaf(s0, P.scale_log2, -mref));
-            const float p1 = ex2(fmaf(s1, P.scale_log2, -mref));
-            psum += p0 + p1;
-            pk[x] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(tS + ch * 16, pk);
-        }
+        const float psum = need_mask ? exp_row_to_tmem<true>(tS, vis_max, P.scale_log2, mref)
+                                     : exp_row_to_tmem<false>(tS, vis_max, P.scale_log2, mref);
         l += psum;
         tmem_st_wait();
         tc_fence_before();
@@ -474,6 +552,7 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         uint32_t r[32];
         tmem_ld32(tO + ch * 32, r);
         tmem_ld_wait();
+        reg_fence(r);
         if (valid) {
           if (P.a.out_f32) {
             float4* dst = (float4*)((float*)P.a.o + orow * kD + ch * 32);
