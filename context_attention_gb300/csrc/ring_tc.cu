@@ -239,13 +239,36 @@ __device__ __forceinline__ float row_max_from_tmem(uint32_t tS, int vis_max) {
   return chunk_max<kMask>(rb, 96, vis_max, mx);
 }
 
+// Packed fp32 pair arithmetic (one instruction for two lanes of data), used
+// to keep the softmax's instruction count low: the softmax warps share issue
+// slots with the single thread that issues the tensor-core MMAs.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // 32 scores -> 16 packed bf16 pairs of p = 2^(s*sl2 - ref), written to TMEM
-// columns [16*ch, 16*ch + 16) of the row; returns the chunk's sum of p.
+// columns [16*ch, 16*ch + 16) of the row; adds the chunk's p into `sum2`
+// (two partial sums, one per element of each pair).
 template <bool kMask>
-__device__ __forceinline__ float exp_chunk(const uint32_t (&r)[32], int ch, int vis_max, float sl2,
-                                           float ref, uint32_t tS) {
+__device__ __forceinline__ void exp_chunk(const uint32_t (&r)[32], int ch, int vis_max,
+                                          uint64_t sl2_2, uint64_t nref_2, uint64_t& sum2,
+                                          uint32_t tS) {
   uint32_t pk[16];
-  float s_even = 0.f, s_odd = 0.f;
 #pragma unroll
   for (int x = 0; x < 16; ++x) {
     float s0 = __uint_as_float(r[2 * x]), s1 = __uint_as_float(r[2 * x + 1]);
@@ -253,14 +276,13 @@ __device__ __forceinline__ float exp_chunk(const uint32_t (&r)[32], int ch, int 
       if (ch * 32 + 2 * x > vis_max) s0 = -INFINITY;
       if (ch * 32 + 2 * x + 1 > vis_max) s1 = -INFINITY;
     }
-    const float p0 = ex2(fmaf(s0, sl2, -ref));
-    const float p1 = ex2(fmaf(s1, sl2, -ref));
-    s_even += p0;
-    s_odd += p1;
+    float a0, a1;
+    f2_unpack(f2_fma(f2_pack(s0, s1), sl2_2, nref_2), a0, a1);
+    const float p0 = ex2(a0), p1 = ex2(a1);
+    sum2 = f2_add(sum2, f2_pack(p0, p1));
     pk[x] = pack_bf16x2(p0, p1);
   }
   tmem_st16(tS + ch * 16, pk);
-  return s_even + s_odd;
 }
 
 // Pass 2 over one S row: exp, row sum, P (bf16) back into TMEM, with the
@@ -269,24 +291,27 @@ __device__ __forceinline__ float exp_chunk(const uint32_t (&r)[32], int ch, int 
 template <bool kMask>
 __device__ __forceinline__ float exp_row_to_tmem(uint32_t tS, int vis_max, float sl2, float ref) {
   uint32_t ra[32], rb[32];
-  float sum = 0.f;
+  const uint64_t sl2_2 = f2_pack(sl2, sl2), nref_2 = f2_pack(-ref, -ref);
+  uint64_t sum2 = f2_pack(0.f, 0.f);
   tmem_ld32(tS, ra);
   tmem_ld_wait();
   reg_fence(ra);
   tmem_ld32(tS + 32, rb);
-  sum += exp_chunk<kMask>(ra, 0, vis_max, sl2, ref, tS);
+  exp_chunk<kMask>(ra, 0, vis_max, sl2_2, nref_2, sum2, tS);
   tmem_ld_wait();
   reg_fence(rb);
   tmem_ld32(tS + 64, ra);
-  sum += exp_chunk<kMask>(rb, 1, vis_max, sl2, ref, tS);
+  exp_chunk<kMask>(rb, 1, vis_max, sl2_2, nref_2, sum2, tS);
   tmem_ld_wait();
   reg_fence(ra);
   tmem_ld32(tS + 96, rb);
-  sum += exp_chunk<kMask>(ra, 2, vis_max, sl2, ref, tS);
+  exp_chunk<kMask>(ra, 2, vis_max, sl2_2, nref_2, sum2, tS);
   tmem_ld_wait();
   reg_fence(rb);
-  sum += exp_chunk<kMask>(rb, 3, vis_max, sl2, ref, tS);
-  return sum;
+  exp_chunk<kMask>(rb, 3, vis_max, sl2_2, nref_2, sum2, tS);
+  float lo, hi;
+  f2_unpack(sum2, lo, hi);
+  return lo + hi;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
