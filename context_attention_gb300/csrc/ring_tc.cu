@@ -159,28 +159,70 @@ struct TileIter {
   }
 };
 
-__device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sbase, int i, int slot) {
-  const uint32_t d = tmem + kColS + 128u * i;
-  const uint32_t qa = sbase + kSmemQ + i * kTileBytes;
-  const uint32_t ka = sbase + kSmemKV + slot * kTileBytes;
-#pragma unroll
-  for (int kk = 0; kk < kD / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-    tc_mma_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-              kIdescS, kk > 0);
-  }
+// S_i = Q_i K^T: eight K=16 MMAs.  Both operands are K-major 128-byte
+// swizzled tiles stored as two 64-column halves, so the k-th MMA starts 32 B
+// further along inside a half (+2 in 16-byte descriptor units) and the second
+// half 16 KB further (+1024).  All eight issue from one asm block with the
+// descriptors advanced by 64-bit adds, keeping the issuing thread's own
+// instruction count (and so its share of contended issue slots) small.
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc) {
+  asm volatile(
+      "{\n\t"
+      ".reg .pred pf, pt;\n\t"
+      ".reg .b64 a, b;\n\t"
+      "setp.ne.b32 pf, %3, %3;\n\t"
+      "setp.eq.b32 pt, %3, %3;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+      "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 1024;\n\tadd.s64 b, %2, 1024;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 1026;\n\tadd.s64 b, %2, 1026;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 1028;\n\tadd.s64 b, %2, 1028;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "add.s64 a, %1, 1030;\n\tadd.s64 b, %2, 1030;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "}" ::"r"(d_tmem),
+      "l"(qdesc), "l"(kdesc), "n"(kIdescS)
+      : "memory");
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t sbase, int i, int slot,
-                                         bool acc) {
-  const uint32_t d = tmem + kColO + 128u * i;
-  const uint32_t p = tmem + kColS + 128u * i;
-  const uint32_t va = sbase + kSmemKV + slot * kTileBytes;
-#pragma unroll
-  for (int kk = 0; kk < kBN / 16; ++kk) {
-    tc_mma_ts(d, p + kk * 8, smem_desc_sw128(va + kk * 2048, kBoxBytes, 1024), kIdescPV,
-              (acc || kk > 0) ? 1u : 0u);
-  }
+// O_i (+)= P_i V: eight K=16 MMAs with P (bf16, two values per 32-bit TMEM
+// column) as the TMEM A operand, +8 columns per MMA, and V as the MN-major
+// B operand, +16 rows = +2048 B (+128 descriptor units) per MMA.
+// `acc` = 0 makes the first MMA overwrite O (first tile of a unit).
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc,
+                                         uint32_t acc) {
+  asm volatile(
+      "{\n\t"
+      ".reg .pred pa, pt;\n\t"
+      ".reg .b64 b;\n\t"
+      ".reg .b32 a;\n\t"
+      "setp.ne.b32 pa, %3, 0;\n\t"
+      "setp.eq.b32 pt, %3, %3;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, pa;\n\t"
+      "add.s32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "add.s32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "add.s32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "add.s32 a, %1, 32;\n\tadd.s64 b, %2, 512;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "add.s32 a, %1, 40;\n\tadd.s64 b, %2, 640;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "add.s32 a, %1, 48;\n\tadd.s64 b, %2, 768;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "add.s32 a, %1, 56;\n\tadd.s64 b, %2, 896;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "}" ::"r"(d_tmem),
+      "r"(p_tmem), "l"(vdesc), "r"(acc), "n"(kIdescPV)
+      : "memory");
 }
 
 // Orders every use of registers filled by tcgen05.ld after the wait::ld that
@@ -331,7 +373,7 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     *abort_flag = 0;
     for (int s = 0; s < kNSlot; ++s) {
       mbar_init(bar(kBarKvFull + s), 1);
-      mbar_init(bar(kBarKvEmpty + s), 1);
+      mbar_init(bar(kBarKvEmpty + s), 1);  // arrived by softmax warpgroup 1
     }
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
@@ -408,6 +450,15 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
       uint32_t uc = 0;
       uint64_t pos = 0, gt = 0;
       bool ok = true;
+      // base descriptors; a slot's tiles are kTileBytes (2048 units) apart
+      const uint64_t qdesc0 = smem_desc_sw128(sbase + kSmemQ, 16, 1024);
+      const uint64_t qdesc1 = smem_desc_sw128(sbase + kSmemQ + kTileBytes, 16, 1024);
+      const uint64_t kvdesc = smem_desc_sw128(sbase + kSmemKV, 16, 1024);
+      const uint64_t vdesc = smem_desc_sw128(sbase + kSmemKV, kBoxBytes, 1024);
+      auto kd = [&](int slot) { return kvdesc + (uint64_t)(slot * (kTileBytes >> 4)); };
+      auto vd = [&](int slot) { return vdesc + (uint64_t)(slot * (kTileBytes >> 4)); };
+      const uint32_t tS0 = tmem + kColS, tS1 = tmem + kColS + 128, tO0 = tmem + kColO,
+                     tO1 = tmem + kColO + 128;
       for (int64_t u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
         const Unit U = unit_of(P, u);
         const int n = unit_tiles(P, U);
@@ -419,12 +470,10 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         ok = mbar_wait(bar(kBarKvFull + kslot), (uint32_t)((pos / kNSlot) & 1), abort_flag, err);
         if (!ok) break;
         tc_fence_after();
-        issue_s(tmem, sbase, 0, kslot);
+        issue_s(tS0, qdesc0, kd(kslot));
         tc_commit(bar(kBarSFull + 0));
-        issue_s(tmem, sbase, 1, kslot);
+        issue_s(tS1, qdesc1, kd(kslot));
         tc_commit(bar(kBarSFull + 1));
-        if (n == 1) tc_commit(bar(kBarQEmpty));
-        tc_commit(bar(kBarKvEmpty + kslot));
         ++pos;
         for (int j = 0; j < n && ok; ++j) {
           const int vslot = (int)(pos % kNSlot);
@@ -434,7 +483,7 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
           ok = mbar_wait(bar(kBarPFull + 0), pph, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(tmem, sbase, 0, vslot, j > 0);
+          issue_pv(tO0, tS0, vd(vslot), j > 0);
           ++pos;
           const bool more = j + 1 < n;
           if (more) {
@@ -442,7 +491,7 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             ok = mbar_wait(bar(kBarKvFull + kslot), (uint32_t)((pos / kNSlot) & 1), abort_flag, err);
             if (!ok) break;
             tc_fence_after();
-            issue_s(tmem, sbase, 0, kslot);
+            issue_s(tS0, qdesc0, kd(kslot));
             tc_commit(bar(kBarSFull + 0));
           } else {
             tc_commit(bar(kBarOFull + 0));
@@ -450,13 +499,10 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
           ok = mbar_wait(bar(kBarPFull + 1), pph, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(tmem, sbase, 1, vslot, j > 0);
-          tc_commit(bar(kBarKvEmpty + vslot));
+          issue_pv(tO1, tS1, vd(vslot), j > 0);
           if (more) {
-            issue_s(tmem, sbase, 1, kslot);
+            issue_s(tS1, qdesc1, kd(kslot));
             tc_commit(bar(kBarSFull + 1));
-            if (j + 1 == n - 1) tc_commit(bar(kBarQEmpty));
-            tc_commit(bar(kBarKvEmpty + kslot));
             ++pos;
           } else {
             tc_commit(bar(kBarOFull + 1));
@@ -475,6 +521,14 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     const uint32_t tS = tmem + lane_base + kColS + 128u * i;
     const uint32_t tO = tmem + lane_base + kColO + 128u * i;
     const bool const_max = P.a.mode == 1;
+    // Softmax warpgroup 1's first thread releases the K/V ring slots and the
+    // Q tiles: the issuing thread commits s_full[1] after S1(j), which it
+    // issues after S0(j), PV0(j-1) and PV1(j-1), so once s_full[1] of tile j
+    // has completed, K_j, V_(j-1) and (on the last tile) Q are no longer read
+    // by any MMA.  Moving these arrivals off the issuing thread saves it two
+    // commits per tile.
+    const bool releaser = (i == 1 && tid == 0);
+    uint64_t kvpos = 0;  // ring position of K_0 of the current unit
     uint32_t uc = 0;
     uint64_t gt = 0;
     bool ok = true;
@@ -509,6 +563,12 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                         mbar_wait(bar(kBarSFull + i), (uint32_t)((gt + j) & 1), abort_flag, err));
         if (!ok) break;
         tc_fence_after();
+        if (releaser) {
+          const uint64_t kp = kvpos + 2 * (uint64_t)j;  // K_j
+          mbar_arrive(bar(kBarKvEmpty + (int)(kp % kNSlot)));
+          if (j > 0) mbar_arrive(bar(kBarKvEmpty + (int)((kp - 1) % kNSlot)));  // V_(j-1)
+          if (j == n - 1) mbar_arrive(bar(kBarQEmpty));
+        }
         // last visible column of this tile for this row
         const int64_t b0 = (int64_t)it.kt * kBN;
         int64_t lim = P.a.Ls - 1 - b0;
@@ -561,6 +621,8 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + i), uc & 1, abort_flag, err));
       if (!ok) break;
       tc_fence_after();
+      if (releaser) mbar_arrive(bar(kBarKvEmpty + (int)((kvpos + 2 * (uint64_t)n - 1) % kNSlot)));  // V_(n-1)
+      kvpos += 2 * (uint64_t)n;
       float inv, lse;
       if (const_max) {
         inv = P.a.unnormalized ? 1.f : 1.f / fmaxf(l, 1e-37f);
