@@ -314,6 +314,49 @@ class OracleSampler:
                     f"{t:.1f} s on {threads} threads", seconds=t)
 
 
+def bench_other_workloads(ca, torch, reps=5):
+    """Device time of the other ring-attention workloads (online max, sink
+    keys, causal GQA in both layouts) with the same CUDA-event method; each
+    is reported with its algorithmic TFLOP/s (causal counts visible pairs)."""
+    from context_attention_gb300 import synth
+
+    res = {}
+    stream = torch.cuda.current_stream()
+
+    def run(name, q, k, v, cp, mode, causal, layout, flops):
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], device="cuda", dtype=torch.float32)
+        ws = torch.empty(max(16, ca.ring_attn_fwd_workspace_size(q.shape[0], q.shape[1], k.shape[1], q.shape[2],
+                                                                 q.shape[3], cp, mode)), dtype=torch.uint8,
+                         device="cuda")
+        for _ in range(3):
+            ca.ring_attn_fwd(q, k, v, cp, mode=mode, causal=causal, layout=layout, out=out, lse=lse, workspace=ws)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            ca.ring_attn_fwd(q, k, v, cp, mode=mode, causal=causal, layout=layout, out=out, lse=lse, workspace=ws)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        res[name] = {"ms": round(ms, 3), "tflops": round(flops / (ms / 1e3) / 1e12, 1)}
+
+    q, k, v = synth.normal_qkv(2, 32, 32, 32768, 128, 3, dtype=torch.bfloat16, device="cuda")
+    f = 4.0 * 2 * 32 * 32768 ** 2 * 128
+    run("online_max B2 H32 S32768 cp8", q, k, v, 8, "online_max", False, "contiguous", f)
+    run("const_max B2 H32 S32768 cp8", q, k, v, 8, "const_max", False, "contiguous", f)
+    k = synth.apply_sinks(k, synth.sink_rows(2, 32768, seed=33, device="cuda"))
+    run("online_max sinks B2 H32 S32768 cp8", q, k, v, 8, "online_max", False, "contiguous", f)
+    del q, k, v
+    q, k, v = synth.normal_qkv(1, 32, 8, 65536, 128, 4, dtype=torch.bfloat16, device="cuda")
+    f = 4.0 * 32 * 128 * 65536 * 65537 / 2
+    run("causal GQA contiguous Hq32 Hkv8 S65536 cp8", q, k, v, 8, "online_max", True, "contiguous", f)
+    run("causal GQA striped Hq32 Hkv8 S65536 cp8", q, k, v, 8, "online_max", True, "striped", f)
+    del q, k, v
+    torch.cuda.empty_cache()
+    return res
+
+
 def cpu_baseline_prefill(seconds=15.0):
     smp = OracleSampler()
     return smp.measure(smp.rows_for(seconds))
@@ -407,6 +450,8 @@ def run_ours(args):
                                       "traffic": read_traffic("dcp_decode_kernel_131k.txt"),
                                       "peak_source": f"{peak_src} copy bandwidth"},
                          "clocks": dec["clocks"]}
+    if args.other_workloads:
+        out["other_workloads"] = bench_other_workloads(ca, torch)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_prefill(seconds=args.cpu_seconds)
     if rank == 0:
@@ -465,6 +510,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--other-workloads", action="store_true",
+                    help="also time the online-max, sink and causal GQA workloads (reported, not the value)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile", choices=["ring", "decode"], default=None,

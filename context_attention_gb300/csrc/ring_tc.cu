@@ -100,18 +100,34 @@ struct Unit {
   int64_t qrow0;  // first local query row of the unit
 };
 
+// Units of one (batch, head) are consecutive (their K/V stay hot in L2) and
+// heaviest first: contiguous causal work grows with the shard index and then
+// the row block; striped causal work grows with the row block only (every
+// shard pair has a diagonal); non-causal units are all equal.
 __device__ __forceinline__ Unit unit_of(const TcParams& P, int64_t u) {
   Unit U;
   U.bh = u / P.per_head;
-  // heaviest units of a head first (causal work grows with the shard and row)
   const int64_t rem = P.per_head - 1 - (u % P.per_head);
-  U.r_store = (int)(rem / P.qblocks);
-  U.qrow0 = (rem % P.qblocks) * kUnitRows;
+  if (P.a.causal && P.a.layout == kLayoutContiguous) {
+    U.r_store = (int)(rem / P.qblocks);
+    U.qrow0 = (rem % P.qblocks) * kUnitRows;
+  } else {
+    U.r_store = (int)(rem % P.a.q_shards);
+    U.qrow0 = (rem / P.a.q_shards) * kUnitRows;
+  }
   U.b = (int)(U.bh / P.a.Hq);
   U.h = (int)(U.bh % P.a.Hq);
   U.bhk = (int64_t)U.b * P.a.Hkv + U.h / (P.a.Hq / P.a.Hkv);
   U.r_log = P.a.q_rank_fixed >= 0 ? P.a.q_rank_fixed : U.r_store;
   return U;
+}
+
+// The k-th unit of this CTA: units are dealt to CTAs in a snake order
+// (0..G-1, then G-1..0, ...) which, on a heaviest-first unit list, evens out
+// the per-CTA work of causal runs.  Returns >= P.units when none is left.
+__device__ __forceinline__ int64_t unit_at(const TcParams& P, int64_t k) {
+  const int64_t G = gridDim.x;
+  return k * G + ((k & 1) ? (G - 1 - (int64_t)blockIdx.x) : (int64_t)blockIdx.x);
 }
 
 // Key tiles of ring step t that can be visible to some row of the unit.
@@ -404,7 +420,7 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
       uint32_t uc = 0;
       uint64_t pos = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+      for (int64_t k = 0, u = unit_at(P, 0); u < P.units && ok; ++k, u = unit_at(P, k)) {
         const Unit U = unit_of(P, u);
         const int n = unit_tiles(P, U);
         if (n == 0) continue;
@@ -459,7 +475,7 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
       auto vd = [&](int slot) { return vdesc + (uint64_t)(slot * (kTileBytes >> 4)); };
       const uint32_t tS0 = tmem + kColS, tS1 = tmem + kColS + 128, tO0 = tmem + kColO,
                      tO1 = tmem + kColO + 128;
-      for (int64_t u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+      for (int64_t k = 0, u = unit_at(P, 0); u < P.units && ok; ++k, u = unit_at(P, k)) {
         const Unit U = unit_of(P, u);
         const int n = unit_tiles(P, U);
         if (n == 0) continue;
@@ -532,7 +548,7 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     uint32_t uc = 0;
     uint64_t gt = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+    for (int64_t k = 0, u = unit_at(P, 0); u < P.units && ok; ++k, u = unit_at(P, k)) {
       const Unit U = unit_of(P, u);
       const int n = unit_tiles(P, U);
       const int64_t a_row = U.qrow0 + (int64_t)i * kBM + tid;
