@@ -1,0 +1,58 @@
+"""The multi-rank logic of bench.py on CPU: world size 2 over gloo.
+
+Every rank runs an independent replica of the workload; the job time is the
+slowest rank's (max over ranks) and the value aggregates the work of all
+ranks over that time."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+
+    bench.barrier(dist)
+    t = bench.max_over_ranks(10.0 + 5.0 * rank, dist)
+    v = bench.aggregate_throughput(2.0, 4, world, t)
+    q.put((rank, t, v))
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_and_aggregate():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(world))
+    for rank, t, v in res:
+        assert t == 15.0  # slowest rank's time on every rank
+        assert v == pytest.approx(2 * 2.0 * 4 / 0.015)
+
+
+def test_single_rank_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.max_over_ranks(3.5, None) == 3.5
+    assert bench.aggregate_throughput(1e12, 10, 1, 1000.0) == pytest.approx(1e13)
