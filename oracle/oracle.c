@@ -21,7 +21,9 @@
  *    (partial attention + LSE, weight_i = exp(local_lse - global_lse)),
  *    "local_filled Computation", "Active Token Handling and dcp_active_mask",
  *    "Slot Mapping and KV Cache" (block b of I tokens lives on rank b mod W)
- *    and "Segmented Attention CP" (local slot s -> global (s//I)*(W*I)+R*I+s%I).
+ *    and "Segmented Attention CP" (local slot s -> global (s//I)*(W*I)+R*I+s%I;
+ *    chunked prefill against prior + current local KV, causal by global
+ *    position, then the LSE merge).
  *  - "Sharding the Input" (striped layout: token t on device t mod cp;
  *    causal masking: a later token never influences an earlier one).
  *
@@ -396,6 +398,97 @@ void ora_dcp_decode(const float *q, const float *k_shards,
     free(op);
     free(lp);
   }
+}
+
+/* DCP prefill of one chunk ("DCP (Decode Context Parallelism)", section
+ * "Segmented Attention CP"): every rank R holds, locally, the prior tokens
+ * dealt to it (prior slots) and its share of the current chunk (current
+ * tokens).  The gathered queries of the chunk attend to each rank's local
+ * prior + current KV with a causal mask on global positions, giving a
+ * partial (o_R, lse_R); the partials are LSE-merged.
+ *
+ * Global positions, as the page's algorithm step 3 defines them: prior
+ * tokens are the positions [0, P) dealt from position 0; current chunk
+ * token j of rank R sits at P + (chunk position of j), the chunk's own
+ * positions dealt from the chunk start; query i of the chunk sits at P + i.
+ * Both deals are simulated token by token (ora_dcp_deal).
+ *
+ * q [Hq, Sc, D]; k_prior, v_prior [W, Hkv, Lcap, D] (slot s of rank R in
+ * row s); k_cur, v_cur [W, Hkv, Lc, D] (current token j of rank R in row j).
+ * o [Hq, Sc, D], lse [Hq, Sc].  If part_rank >= 0 only that rank's partial
+ * is computed (no merge). */
+void ora_dcp_prefill(const float *q, const float *k_prior, const float *v_prior,
+                     const float *k_cur, const float *v_cur, int Hq, int Hkv,
+                     int64_t Sc, int D, int W, int I, int64_t P, int64_t Lcap,
+                     int64_t Lc, double scale, int part_rank, double *o,
+                     double *lse) {
+  int G = Hq / Hkv;
+  int32_t *own_p = (int32_t *)malloc(sizeof(int32_t) * (size_t)(P > 0 ? P : 1));
+  int64_t *loc_p = (int64_t *)malloc(sizeof(int64_t) * (size_t)(P > 0 ? P : 1));
+  int32_t *own_c = (int32_t *)malloc(sizeof(int32_t) * (size_t)(Sc > 0 ? Sc : 1));
+  int64_t *loc_c = (int64_t *)malloc(sizeof(int64_t) * (size_t)(Sc > 0 ? Sc : 1));
+  ora_dcp_deal(P, W, I, own_p, loc_p);
+  ora_dcp_deal(Sc, W, I, own_c, loc_c);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t hi = 0; hi < (int64_t)Hq * Sc; ++hi) {
+    int64_t h = hi / Sc, i = hi % Sc, hk = h / G;
+    const float *qrow = q + hi * D;
+    double *op = (double *)calloc((size_t)W * D, sizeof(double));
+    double *lp = (double *)malloc(sizeof(double) * (size_t)W);
+    for (int r = 0; r < W; ++r) {
+      lp[r] = -INFINITY;
+      if (part_rank >= 0 && r != part_rank) continue;
+      const float *kp = k_prior + ((int64_t)r * Hkv + hk) * Lcap * D;
+      const float *vp = v_prior + ((int64_t)r * Hkv + hk) * Lcap * D;
+      const float *kc = k_cur + ((int64_t)r * Hkv + hk) * Lc * D;
+      const float *vc = v_cur + ((int64_t)r * Hkv + hk) * Lc * D;
+      /* visible keys of rank r: its prior tokens (all before the chunk) and
+       * its current tokens at chunk positions <= i */
+      double m = -INFINITY;
+      for (int pass = 0; pass < 2; ++pass) {
+        double l = 0.0;
+        for (int64_t p = 0; p < P + i + 1; ++p) {
+          const float *kr, *vr;
+          if (p < P) {
+            if (own_p[p] != r) continue;
+            kr = kp + loc_p[p] * D;
+            vr = vp + loc_p[p] * D;
+          } else {
+            if (own_c[p - P] != r) continue;
+            kr = kc + loc_c[p - P] * D;
+            vr = vc + loc_c[p - P] * D;
+          }
+          double dot = 0.0;
+          for (int d = 0; d < D; ++d) dot += (double)qrow[d] * (double)kr[d];
+          double sj = scale * dot;
+          if (pass == 0) {
+            if (sj > m) m = sj;
+          } else {
+            double w = exp(sj - m);
+            l += w;
+            for (int d = 0; d < D; ++d) op[(int64_t)r * D + d] += w * (double)vr[d];
+          }
+        }
+        if (pass == 0 && m == -INFINITY) break;
+        if (pass == 1) {
+          for (int d = 0; d < D; ++d) op[(int64_t)r * D + d] /= l;
+          lp[r] = m + log(l);
+        }
+      }
+    }
+    if (part_rank >= 0) {
+      for (int d = 0; d < D; ++d) o[hi * D + d] = op[(int64_t)part_rank * D + d];
+      lse[hi] = lp[part_rank];
+    } else {
+      ora_lse_merge(op, lp, W, 1, D, o + hi * D, lse + hi);
+    }
+    free(op);
+    free(lp);
+  }
+  free(own_p);
+  free(loc_p);
+  free(own_c);
+  free(loc_c);
 }
 
 /* Number of OpenMP threads a parallel region here would use. */

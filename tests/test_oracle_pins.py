@@ -341,3 +341,64 @@ def test_dcp_decode_zero_query_closed_form():
     for n in range(N):
         np.testing.assert_allclose(o[n], np.broadcast_to(vg[n, 0, : seq_lens[n]].astype(np.float64).mean(0), (Hq, D)), atol=1e-12)
         np.testing.assert_allclose(lse[n], math.log(seq_lens[n]), atol=1e-12)
+
+
+# ---------------------------------------------------------------- DCP prefill
+
+
+def _dcp_prefill_shards(kg, P, Sc, W, I, Lcap):
+    """Split a global K [Hkv, P+Sc, D] into prior shards [W,Hkv,Lcap,D] (prior
+    slot s of rank R = global (s//I)*(W*I) + R*I + s%I) and current shards
+    [W,Hkv,Sc/W,D] (chunk token j of rank R = global P + (j//I)*(W*I) + R*I + j%I),
+    both maps as the DCP page's "Segmented Attention CP" step 3 prints them."""
+    Hkv, L, D = kg.shape
+    prior = np.full((W, Hkv, Lcap, D), 1e3, np.float32)  # unused slots: junk that must never be read
+    cur = np.zeros((W, Hkv, Sc // W, D), np.float32)
+    for R in range(W):
+        for s in range(Lcap):
+            g = (s // I) * (W * I) + R * I + s % I
+            if g < P:
+                prior[R, :, s] = kg[:, g]
+        for j in range(Sc // W):
+            cur[R, :, j] = kg[:, P + (j // I) * (W * I) + R * I + j % I]
+    return prior, cur
+
+
+@pytest.mark.parametrize("P", [0, 16, 64, 77])
+def test_dcp_prefill_equals_causal_attention_over_prefix(P):
+    """A chunk of Sc new tokens after P cached ones, split over W ranks:
+    the merged result equals plain causal attention of the chunk's queries
+    (global positions P..P+Sc-1) over the whole global sequence."""
+    Hq, Hkv, D, W, I, Sc = 4, 2, 8, 4, 4, 32
+    L = P + Sc
+    Lcap = 40
+    q = rnd(Hq, Sc, D)
+    kg, vg = rnd(Hkv, L, D), rnd(Hkv, L, D)
+    kp, kc = _dcp_prefill_shards(kg, P, Sc, W, I, Lcap)
+    vp, vc = _dcp_prefill_shards(vg, P, Sc, W, I, Lcap)
+    o, lse = ora.dcp_prefill(q, kp, vp, kc, vc, I, P)
+    qfull = np.zeros((1, Hq, L, D), np.float32)
+    qfull[0, :, P:] = q
+    rows = [h * L + P + i for h in range(Hq) for i in range(Sc)]
+    ro, rl = ora.attention(qfull, kg[None], vg[None], causal=True, rows=rows)
+    np.testing.assert_allclose(o.reshape(-1, D), ro, atol=1e-12)
+    np.testing.assert_allclose(lse.reshape(-1), rl, atol=1e-12)
+    # per-rank partials, LSE-merged, give the same (page steps 4-7)
+    parts = [ora.dcp_prefill(q, kp, vp, kc, vc, I, P, part_rank=R) for R in range(W)]
+    mo, ml = ora.lse_merge(np.stack([p[0].reshape(-1, D) for p in parts]), np.stack([p[1].reshape(-1) for p in parts]))
+    np.testing.assert_allclose(mo, ro, atol=1e-12)
+    np.testing.assert_allclose(ml, rl, atol=1e-12)
+
+
+def test_dcp_prefill_zero_query_prefix_means():
+    """q = 0: the chunk query at global position P+i gets the mean of v over
+    positions 0..P+i and lse = ln(P+i+1)."""
+    Hq, Hkv, D, W, I, Sc, P = 2, 1, 4, 2, 4, 16, 24
+    q = np.zeros((Hq, Sc, D), np.float32)
+    kg, vg = rnd(Hkv, P + Sc, D), rnd(Hkv, P + Sc, D)
+    kp, kc = _dcp_prefill_shards(kg, P, Sc, W, I, 16)
+    vp, vc = _dcp_prefill_shards(vg, P, Sc, W, I, 16)
+    o, lse = ora.dcp_prefill(q, kp, vp, kc, vc, I, P)
+    for i in range(Sc):
+        np.testing.assert_allclose(o[:, i], np.broadcast_to(vg[0, : P + i + 1].astype(np.float64).mean(0), (Hq, D)), atol=1e-12)
+        np.testing.assert_allclose(lse[:, i], math.log(P + i + 1), atol=1e-12)
