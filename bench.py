@@ -395,6 +395,26 @@ def bench_other_workloads(ca, torch, reps=5):
     run("causal GQA striped Hq32 Hkv8 S65536 cp8", q, k, v, 8, "online_max", True, "striped", f)
     del q, k, v
     torch.cuda.empty_cache()
+    # DCP prefill: an 8192-token chunk after 122880 cached tokens, dcp=4, I=16
+    Hq, Hkv, W, I, Sc, P = 32, 8, 4, 16, 8192, 122880
+    q, kp, vp, kc, vc = synth.dcp_prefill_inputs(Hq, Hkv, 128, W, Sc, P // W, Sc // W, 6, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty(Hq, Sc, device="cuda", dtype=torch.float32)
+    for _ in range(3):
+        ca.dcp_prefill(q, kp, vp, kc, vc, I, P, out=out, lse=lse)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        ca.dcp_prefill(q, kp, vp, kc, vc, I, P, out=out, lse=lse)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    f = 4.0 * 128 * Hq * (Sc * P + Sc * (Sc + 1) / 2)
+    res["dcp_prefill Hq32 Hkv8 chunk8192 prior122880 dcp4"] = {"ms": round(ms, 3),
+                                                               "tflops": round(f / (ms / 1e3) / 1e12, 1)}
+    del q, kp, vp, kc, vc
+    torch.cuda.empty_cache()
     return res
 
 

@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "CtxAttnError", "build", "library_path", "ring_attn_fwd", "ring_attn_fwd_bounded", "attn_partial_step", "lse_merge",
-    "const_max_bound", "dcp_decode", "dcp_decode_noalloc", "layout_to_shards", "layout_from_shards", "dcp_shard_kv",
+    "const_max_bound", "dcp_decode", "dcp_decode_noalloc", "dcp_prefill", "dcp_prefill_partial", "layout_to_shards", "layout_from_shards", "dcp_shard_kv",
     "layout_global_index", "layout_shard_row", "ring_kv_shard", "dcp_owner", "dcp_local_index",
     "dcp_local_to_global", "dcp_local_filled", "dcp_active_mask", "dcp_slot_mapping",
     "device_status", "ring_attn_fwd_workspace_size", "dcp_decode_workspace_size",
@@ -78,6 +78,8 @@ def _load():
             "ca_dcp_decode_workspace_size": ([I, I, I, I64, I, I, I], SZ),
             "ca_dcp_decode": ([P, P, P, I, I, I, I, I64, I, I, I, P, F, P, P, P, SZ, P], I),
             "ca_dcp_decode_noalloc": ([P, P, P, I, I, I, I, I64, I, I, I, P, F, P, P, P], I),
+            "ca_dcp_prefill": ([P, P, P, P, P, I, I, I, I64, I, I, I, I64, I64, I64, F, P, P, P], I),
+            "ca_dcp_prefill_partial": ([P, P, P, P, P, I, I, I, I64, I, I, I, I64, I64, I64, I, F, P, P, P], I),
             "ca_layout_to_shards": ([P, P, I64, I64, I64, I, I, P], I),
             "ca_layout_from_shards": ([P, P, I64, I64, I64, I, I, P], I),
             "ca_dcp_shard_kv": ([P, P, I64, I64, I64, I, I, P], I),
@@ -285,6 +287,46 @@ def dcp_decode_noalloc(q, k_shards, v_shards, interleave, seq_lens=None, softmax
                                    _ptr(lse), _stream(q))
     _check("ca_dcp_decode_noalloc", st)
     return out, lse
+
+
+def dcp_prefill(q, k_prior, v_prior, k_cur, v_cur, interleave, prior_tokens, softmax_scale=None, out=None,
+                lse=None):
+    """DCP prefill of one chunk (online max).
+
+    q [Hq,Sc,D]; prior shards [dcp,Hkv,Lcap,D]; current shards [dcp,Hkv,Lc,D]
+    (bf16, D=128).  Returns (o [Hq,Sc,D] bf16, lse [Hq,Sc])."""
+    lib = _load()
+    _need(q, "q", 3)
+    for n, t in (("k_prior", k_prior), ("v_prior", v_prior), ("k_cur", k_cur), ("v_cur", v_cur)):
+        _need(t, n, 4)
+    Hq, Sc, D = q.shape
+    W, Hkv, Lcap, _ = k_prior.shape
+    Lc = k_cur.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(Hq, Sc, device=q.device, dtype=torch.float32)
+    st = lib.ca_dcp_prefill(_ptr(q), _ptr(k_prior), _ptr(v_prior), _ptr(k_cur), _ptr(v_cur), DTYPE[q.dtype], Hq,
+                            Hkv, Sc, D, W, interleave, int(prior_tokens), Lcap, Lc, float(softmax_scale or 0.0),
+                            _ptr(out), _ptr(lse), _stream(q))
+    _check("ca_dcp_prefill", st)
+    return out, lse
+
+
+def dcp_prefill_partial(q, k_prior, v_prior, k_cur, v_cur, interleave, prior_tokens, rank, softmax_scale=None):
+    """One rank's DCP prefill partial: (o_part [Hq,Sc,D] fp32, lse_part [Hq,Sc])."""
+    lib = _load()
+    _need(q, "q", 3)
+    Hq, Sc, D = q.shape
+    W, Hkv, Lcap, _ = k_prior.shape
+    Lc = k_cur.shape[2]
+    o = torch.empty(Hq, Sc, D, device=q.device, dtype=torch.float32)
+    lse = torch.empty(Hq, Sc, device=q.device, dtype=torch.float32)
+    st = lib.ca_dcp_prefill_partial(_ptr(q), _ptr(k_prior), _ptr(v_prior), _ptr(k_cur), _ptr(v_cur),
+                                    DTYPE[q.dtype], Hq, Hkv, Sc, D, W, interleave, int(prior_tokens), Lcap, Lc,
+                                    int(rank), float(softmax_scale or 0.0), _ptr(o), _ptr(lse), _stream(q))
+    _check("ca_dcp_prefill_partial", st)
+    return o, lse
 
 
 def _rows(x: torch.Tensor):

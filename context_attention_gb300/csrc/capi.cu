@@ -337,6 +337,76 @@ ca_status ca_dcp_decode(const void* q, const void* k_shards, const void* v_shard
                                    o, 1, lse, s));
 }
 
+// ------------------------------------------------------------------ DCP prefill
+static ca_status dcp_prefill_common(const void* q, const void* k_prior, const void* v_prior,
+                                    const void* k_cur, const void* v_cur, ca_dtype dtype, int Hq,
+                                    int Hkv, int64_t Sc, int D, int dcp, int interleave,
+                                    int64_t prior_tokens, int64_t Lcap, int64_t Lc, int rank,
+                                    float softmax_scale, void* o, int out_f32, float* lse,
+                                    void* stream) {
+  if (!q || !k_prior || !v_prior || !k_cur || !v_cur || !o) return CA_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || Hq <= 0 || Hkv <= 0 || Sc <= 0 || D <= 0 || dcp <= 0 ||
+      interleave <= 0 || prior_tokens < 0 || Lcap <= 0 || Lc <= 0)
+    return CA_ERR_INVALID_ARG;
+  if (rank >= dcp) return CA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return CA_ERR_SHAPE;
+  if (dtype != CA_DTYPE_BF16 || D != 128 || dcp > kDcpPrefillMaxRanks) return CA_ERR_UNSUPPORTED;
+  if (Lcap < dcp_local_filled(prior_tokens, dcp, interleave, interleave, 0) ||
+      Lc < dcp_local_filled(Sc, dcp, interleave, interleave, 0))
+    return CA_ERR_SHAPE;
+  if ((int64_t)Hq * Sc >= ((int64_t)1 << 31) || Lcap >= ((int64_t)1 << 31)) return CA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_prior) || !aligned16(v_prior) || !aligned16(k_cur) ||
+      !aligned16(v_cur) || !aligned16(o) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return CA_ERR_ALIGNMENT;
+  ca_status st = device_is_gb300();
+  if (st != CA_OK) return st;
+  unsigned* err = device_error_word();
+  if (!err) return CA_ERR_CUDA;
+  DcpPrefillArgs d;
+  d.q = q;
+  d.k_prior = k_prior;
+  d.v_prior = v_prior;
+  d.k_cur = k_cur;
+  d.v_cur = v_cur;
+  d.Hq = Hq;
+  d.Hkv = Hkv;
+  d.D = D;
+  d.W = dcp;
+  d.I = interleave;
+  d.Sc = Sc;
+  d.P = prior_tokens;
+  d.Lcap = Lcap;
+  d.Lc = Lc;
+  d.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
+  d.part_rank = rank;
+  d.o = o;
+  d.out_f32 = out_f32;
+  d.lse = lse;
+  d.err = err;
+  return launched(launch_dcp_prefill_tc(d, static_cast<cudaStream_t>(stream)));
+}
+
+ca_status ca_dcp_prefill(const void* q, const void* k_prior, const void* v_prior, const void* k_cur,
+                         const void* v_cur, ca_dtype dtype, int Hq, int Hkv, int64_t Sc, int D,
+                         int dcp, int interleave, int64_t prior_tokens, int64_t Lcap, int64_t Lc,
+                         float softmax_scale, void* o, float* lse, void* stream) {
+  return dcp_prefill_common(q, k_prior, v_prior, k_cur, v_cur, dtype, Hq, Hkv, Sc, D, dcp,
+                            interleave, prior_tokens, Lcap, Lc, -1, softmax_scale, o, 0, lse,
+                            stream);
+}
+
+ca_status ca_dcp_prefill_partial(const void* q, const void* k_prior, const void* v_prior,
+                                 const void* k_cur, const void* v_cur, ca_dtype dtype, int Hq,
+                                 int Hkv, int64_t Sc, int D, int dcp, int interleave,
+                                 int64_t prior_tokens, int64_t Lcap, int64_t Lc, int rank,
+                                 float softmax_scale, float* o_part, float* lse_part,
+                                 void* stream) {
+  if (rank < 0 || !lse_part) return CA_ERR_INVALID_ARG;
+  return dcp_prefill_common(q, k_prior, v_prior, k_cur, v_cur, dtype, Hq, Hkv, Sc, D, dcp,
+                            interleave, prior_tokens, Lcap, Lc, rank, softmax_scale, o_part, 1,
+                            lse_part, stream);
+}
+
 // ------------------------------------------------------------------ layouts
 static ca_status check_rows(const void* a, const void* b, int64_t BH, int64_t S, int64_t row_bytes) {
   if (!a || !b || BH <= 0 || S <= 0 || row_bytes <= 0) return CA_ERR_INVALID_ARG;

@@ -31,6 +31,25 @@ struct RingArgs {
 };
 
 cudaError_t launch_ring_tc_bf16(const RingArgs& a, cudaStream_t stream);
+
+// DCP prefill of one chunk on the tensor-core kernel's segmented schedule.
+struct DcpPrefillArgs {
+  const void* q;        // [Hq, Sc, D]
+  const void* k_prior;  // [W, Hkv, Lcap, D]
+  const void* v_prior;
+  const void* k_cur;    // [W, Hkv, Lc, D]
+  const void* v_cur;
+  int Hq, Hkv, D, W, I;
+  int64_t Sc, P, Lcap, Lc;
+  float scale;
+  int part_rank;        // -1: all ranks merged; else one rank's partial
+  void* o;              // [Hq, Sc, D]: bf16 (merged) or fp32 (partial)
+  int out_f32;
+  float* lse;           // [Hq, Sc] or null
+  unsigned* err;
+};
+constexpr int kDcpPrefillMaxRanks = 8;
+cudaError_t launch_dcp_prefill_tc(const DcpPrefillArgs& d, cudaStream_t stream);
 cudaError_t launch_ring_simt_f32(const RingArgs& a, cudaStream_t stream);
 
 cudaError_t launch_const_max_bound(const void* q, const void* k, int is_bf16, int B,

@@ -81,6 +81,7 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kMaxRanks = 8;               // segmented schedule
 
 struct TcParams {
   RingArgs a;
@@ -90,6 +91,24 @@ struct TcParams {
   int nsteps;
   int nkt;          // key tiles per shard
   float scale_log2;
+  // Segmented schedule (DCP prefill): the keys of rank R come in two
+  // segments -- its prior cache slots [0, lp[R]) and its current-chunk
+  // tokens [0, lc[R]) -- read through per-rank tensor maps; current token j
+  // is visible to query row a iff j <= local_filled(a + 1, W, I, I, R) - 1.
+  int seg;          // 0: ring schedule over virtual shards, 1: segmented
+  int W, I;         // DCP degree and interleave (segmented)
+  int part_rank;    // segmented: -1 = all ranks, else only this rank
+  int64_t lp[kMaxRanks], lc[kMaxRanks];
+};
+
+// Tensor maps of one launch: q, then (K, V) per key source.  The ring
+// schedule uses one 2-D source (all shards of a head, rows of the stored
+// tensor); the segmented schedule uses 3-D sources [Hkv, rows, D] per rank
+// and segment (prior = 2R, current = 2R + 1) whose row extent is the rank's
+// valid count, so TMA fills rows past it with zeros.
+struct TcMaps {
+  CUtensorMap q;
+  CUtensorMap kv[2 * 2 * kMaxRanks];
 };
 
 struct Unit {
@@ -130,47 +149,102 @@ __device__ __forceinline__ int64_t unit_at(const TcParams& P, int64_t k) {
   return k * G + ((k & 1) ? (G - 1 - (int64_t)blockIdx.x) : (int64_t)blockIdx.x);
 }
 
-// Key tiles of ring step t that can be visible to some row of the unit.
-__device__ __forceinline__ int step_tiles(const TcParams& P, const Unit& U, int t,
-                                          int* s_store, int64_t* delta) {
-  const int s_log = P.a.kv_rank_fixed >= 0 ? P.a.kv_rank_fixed : ring_kv_shard(U.r_log, t, P.a.cp);
-  *s_store = P.a.kv_rank_fixed >= 0 ? 0 : s_log;
-  *delta = P.a.causal ? causal_delta(P.a.layout, U.r_log, s_log) : kDeltaAll;
-  if (*delta == kDeltaNone) return 0;
-  if (*delta == kDeltaAll) return P.nkt;
+// One step of a unit's key sequence: which source the keys come from, where
+// they start, how many there are, and how the causal rule limits them.
+enum { kMaskNone = 0, kMaskDelta = 1, kMaskDcp = 2 };
+struct Step {
+  int nk;         // key tiles that can be visible to some row of the unit
+  int src;        // key source: tensor maps kv[2*src] (K), kv[2*src+1] (V)
+  int64_t row0;   // ring: TMA row of key 0; segmented: 0 (rows are per source)
+  int64_t nkeys;  // keys in the step (ragged end)
+  int mask;       // kMaskNone / kMaskDelta / kMaskDcp
+  int64_t delta;  // kMaskDelta: key b visible to row a iff b <= a - delta
+  int rank;       // kMaskDcp: rank whose current tokens these are
+};
+
+__device__ __forceinline__ Step step_info(const TcParams& P, const Unit& U, int t) {
+  Step st;
   const int64_t a_max = min(U.qrow0 + kUnitRows - 1, P.a.Ls - 1);
-  const int64_t bmax = a_max - *delta;
-  if (bmax < 0) return 0;
-  return (int)min((int64_t)P.nkt, bmax / kBN + 1);
+  if (P.seg) {
+    const int R = P.part_rank >= 0 ? P.part_rank : (t >> 1);
+    st.rank = R;
+    st.row0 = 0;
+    st.delta = 0;
+    if ((t & 1) == 0) {  // prior slots: all before the chunk, all visible
+      st.src = 2 * R;
+      st.nkeys = P.lp[R];
+      st.mask = kMaskNone;
+      st.nk = (int)((st.nkeys + kBN - 1) / kBN);
+    } else {             // current chunk tokens of rank R: causal by global position
+      st.src = 2 * R + 1;
+      st.nkeys = P.lc[R];
+      st.mask = kMaskDcp;
+      int64_t jmax = dcp_local_filled(a_max + 1, P.W, P.I, P.I, R) - 1;
+      if (jmax > st.nkeys - 1) jmax = st.nkeys - 1;
+      st.nk = jmax < 0 ? 0 : (int)(jmax / kBN + 1);
+    }
+    return st;
+  }
+  const int s_log = P.a.kv_rank_fixed >= 0 ? P.a.kv_rank_fixed : ring_kv_shard(U.r_log, t, P.a.cp);
+  const int s_store = P.a.kv_rank_fixed >= 0 ? 0 : s_log;
+  st.src = 0;
+  st.rank = 0;
+  st.row0 = U.bhk * P.a.Sk + (int64_t)s_store * P.a.Ls;
+  st.nkeys = P.a.Ls;
+  st.delta = P.a.causal ? causal_delta(P.a.layout, U.r_log, s_log) : kDeltaAll;
+  st.mask = st.delta == kDeltaAll ? kMaskNone : kMaskDelta;
+  if (st.delta == kDeltaNone) {
+    st.nk = 0;
+  } else if (st.delta == kDeltaAll) {
+    st.nk = P.nkt;
+  } else {
+    const int64_t bmax = a_max - st.delta;
+    st.nk = bmax < 0 ? 0 : (int)min((int64_t)P.nkt, bmax / kBN + 1);
+  }
+  return st;
 }
 
 __device__ __forceinline__ int unit_tiles(const TcParams& P, const Unit& U) {
-  int n = 0, s;
-  int64_t d;
-  for (int t = 0; t < P.nsteps; ++t) n += step_tiles(P, U, t, &s, &d);
+  int n = 0;
+  for (int t = 0; t < P.nsteps; ++t) n += step_info(P, U, t).nk;
   return n;
 }
 
-// Walks the (step, key tile) sequence of a unit in ring order.
+// Last key of step `st` visible to query row a (may be < 0: none).
+__device__ __forceinline__ int64_t step_row_limit(const TcParams& P, const Step& st, int64_t a) {
+  int64_t lim = st.nkeys - 1;
+  if (st.mask == kMaskDelta) {
+    lim = min(lim, a - st.delta);
+  } else if (st.mask == kMaskDcp) {
+    lim = min(lim, dcp_local_filled(a + 1, P.W, P.I, P.I, st.rank) - 1);
+  }
+  return lim;
+}
+
+// Walks the (step, key tile) sequence of a unit in order.
 struct TileIter {
-  int t, kt, nk, s_store;
-  int64_t delta;
+  int t, kt;
+  bool new_step;  // true on the first tile of a step
+  Step st;
   __device__ __forceinline__ void seek(const TcParams& P, const Unit& U) {
     while (t < P.nsteps) {
-      nk = step_tiles(P, U, t, &s_store, &delta);
-      if (nk > 0) return;
+      st = step_info(P, U, t);
+      if (st.nk > 0) return;
       ++t;
     }
   }
   __device__ __forceinline__ void begin(const TcParams& P, const Unit& U) {
     t = 0;
     kt = 0;
+    new_step = true;
     seek(P, U);
   }
   __device__ __forceinline__ void next(const TcParams& P, const Unit& U) {
-    if (++kt < nk) return;
+    new_step = false;
+    if (++kt < st.nk) return;
     kt = 0;
     ++t;
+    new_step = true;
     seek(P, U);
   }
 };
@@ -373,8 +447,7 @@ __device__ __forceinline__ float exp_row_to_tmem(uint32_t tS, int vis_max, float
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-               const __grid_constant__ CUtensorMap tv, const TcParams P) {
+ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
@@ -405,9 +478,9 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     tmem_relinquish();
   }
   if (warp == kProducerWarp && lane == 0) {
-    prefetch_tensormap(&tq);
-    prefetch_tensormap(&tk);
-    prefetch_tensormap(&tv);
+    prefetch_tensormap(&maps.q);
+    prefetch_tensormap(&maps.kv[0]);
+    prefetch_tensormap(&maps.kv[1]);
   }
   tc_fence_before();
   __syncthreads();
@@ -430,22 +503,28 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         const int qrow = (int)(U.bh * P.a.Sq + (int64_t)U.r_store * P.a.Ls + U.qrow0);
         for (int i = 0; i < 2; ++i)
           for (int hx = 0; hx < 2; ++hx)
-            tma_load_2d(sbase + kSmemQ + i * kTileBytes + hx * kBoxBytes, &tq, bar(kBarQFull),
+            tma_load_2d(sbase + kSmemQ + i * kTileBytes + hx * kBoxBytes, &maps.q, bar(kBarQFull),
                         hx * 64, qrow + i * kBM);
         TileIter it;
         it.begin(P, U);
         for (int j = 0; j < n && ok; ++j) {
-          const int krow = (int)(U.bhk * P.a.Sk + (int64_t)it.s_store * P.a.Ls + (int64_t)it.kt * kBN);
+          const int krow = (int)(it.st.row0 + (int64_t)it.kt * kBN);
+          const int kvh = (int)(U.bhk);
           for (int kv = 0; kv < 2 && ok; ++kv) {
             const int slot = (int)(pos % kNSlot);
             const uint32_t ph = (uint32_t)((pos / kNSlot) & 1);
             ok = mbar_wait(bar(kBarKvEmpty + slot), ph ^ 1, abort_flag, err);
             if (!ok) break;
             mbar_arrive_expect_tx(bar(kBarKvFull + slot), kTileBytes);
-            const CUtensorMap* m = kv == 0 ? &tk : &tv;
-            for (int hx = 0; hx < 2; ++hx)
-              tma_load_2d(sbase + kSmemKV + slot * kTileBytes + hx * kBoxBytes, m,
-                          bar(kBarKvFull + slot), hx * 64, krow);
+            const CUtensorMap* m = &maps.kv[2 * it.st.src + kv];
+            for (int hx = 0; hx < 2; ++hx) {
+              if (P.seg)
+                tma_load_3d(sbase + kSmemKV + slot * kTileBytes + hx * kBoxBytes, m,
+                            bar(kBarKvFull + slot), hx * 64, krow, kvh);
+              else
+                tma_load_2d(sbase + kSmemKV + slot * kTileBytes + hx * kBoxBytes, m,
+                            bar(kBarKvFull + slot), hx * 64, krow);
+            }
             ++pos;
           }
           it.next(P, U);
@@ -574,6 +653,7 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
       float l = 0.f;
       TileIter it;
       it.begin(P, U);
+      int64_t row_lim = 0;
       for (int j = 0; j < n; ++j) {
         ok = __all_sync(0xffffffffu,
                         mbar_wait(bar(kBarSFull + i), (uint32_t)((gt + j) & 1), abort_flag, err));
@@ -586,9 +666,8 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
           if (j == n - 1) mbar_arrive(bar(kBarQEmpty));
         }
         // last visible column of this tile for this row
-        const int64_t b0 = (int64_t)it.kt * kBN;
-        int64_t lim = P.a.Ls - 1 - b0;
-        if (it.delta != kDeltaAll) lim = min(lim, a_row - it.delta - b0);
+        if (it.new_step) row_lim = step_row_limit(P, it.st, a_row);
+        const int64_t lim = row_lim - (int64_t)it.kt * kBN;
         const int vis_max = (int)max((int64_t)-1, min(lim, (int64_t)(kBN - 1)));
         const bool need_mask = __any_sync(0xffffffffu, vis_max < kBN - 1);
         float mref;
@@ -694,24 +773,7 @@ ring_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 
 }  // namespace
 
-cudaError_t launch_ring_tc_bf16(const RingArgs& a, cudaStream_t stream) {
-  if (a.D != kD) return cudaErrorInvalidValue;
-  TcParams P;
-  P.a = a;
-  P.qblocks = (int)((a.Ls + kUnitRows - 1) / kUnitRows);
-  P.per_head = (int64_t)a.q_shards * P.qblocks;
-  P.units = (int64_t)a.B * a.Hq * P.per_head;
-  P.nsteps = a.kv_rank_fixed >= 0 ? 1 : a.cp;
-  P.nkt = (int)((a.Ls + kBN - 1) / kBN);
-  P.scale_log2 = a.scale * kLog2e;
-  if (P.units == 0) return cudaSuccess;
-
-  CUtensorMap tq, tk, tv;
-  if (!encode_bf16_2d_sw128(&tq, a.q, (uint64_t)a.B * a.Hq * a.Sq, kD, kBM, 64) ||
-      !encode_bf16_2d_sw128(&tk, a.k, (uint64_t)a.B * a.Hkv * a.Sk, kD, kBN, 64) ||
-      !encode_bf16_2d_sw128(&tv, a.v, (uint64_t)a.B * a.Hkv * a.Sk, kD, kBN, 64))
-    return cudaErrorInvalidValue;
-
+static cudaError_t launch_tc(const TcMaps& maps, const TcParams& P, cudaStream_t stream) {
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -723,8 +785,94 @@ cudaError_t launch_ring_tc_bf16(const RingArgs& a, cudaStream_t stream) {
   }
   const int sms = device_sm_count();
   const int64_t grid = P.units < sms ? P.units : sms;
-  ring_tc_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(tq, tk, tv, P);
+  ring_tc_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(maps, P);
   return cudaGetLastError();
+}
+
+static void init_common(TcParams& P, const RingArgs& a) {
+  P.a = a;
+  P.qblocks = (int)((a.Ls + kUnitRows - 1) / kUnitRows);
+  P.per_head = (int64_t)a.q_shards * P.qblocks;
+  P.units = (int64_t)a.B * a.Hq * P.per_head;
+  P.nkt = (int)((a.Ls + kBN - 1) / kBN);
+  P.scale_log2 = a.scale * kLog2e;
+  P.seg = 0;
+  P.W = 1;
+  P.I = 1;
+  P.part_rank = -1;
+  for (int r = 0; r < kMaxRanks; ++r) P.lp[r] = P.lc[r] = 0;
+}
+
+cudaError_t launch_ring_tc_bf16(const RingArgs& a, cudaStream_t stream) {
+  if (a.D != kD) return cudaErrorInvalidValue;
+  TcParams P;
+  init_common(P, a);
+  P.nsteps = a.kv_rank_fixed >= 0 ? 1 : a.cp;
+  if (P.units == 0) return cudaSuccess;
+  TcMaps maps;
+  if (!encode_bf16_2d_sw128(&maps.q, a.q, (uint64_t)a.B * a.Hq * a.Sq, kD, kBM, 64) ||
+      !encode_bf16_2d_sw128(&maps.kv[0], a.k, (uint64_t)a.B * a.Hkv * a.Sk, kD, kBN, 64) ||
+      !encode_bf16_2d_sw128(&maps.kv[1], a.v, (uint64_t)a.B * a.Hkv * a.Sk, kD, kBN, 64))
+    return cudaErrorInvalidValue;
+  return launch_tc(maps, P, stream);
+}
+
+cudaError_t launch_dcp_prefill_tc(const DcpPrefillArgs& d, cudaStream_t stream) {
+  static_assert(kDcpPrefillMaxRanks == kMaxRanks, "rank limit");
+  if (d.D != kD || d.W < 1 || d.W > kMaxRanks) return cudaErrorInvalidValue;
+  RingArgs a;
+  a.q = d.q;
+  a.k = nullptr;
+  a.v = nullptr;
+  a.B = 1;
+  a.Hq = d.Hq;
+  a.Hkv = d.Hkv;
+  a.D = d.D;
+  a.Sq = d.Sc;
+  a.Sk = 0;
+  a.Ls = d.Sc;
+  a.cp = 1;
+  a.q_shards = 1;
+  a.q_rank_fixed = 0;
+  a.kv_rank_fixed = -1;
+  a.causal = 0;  // causality comes from the segments' global positions
+  a.layout = 0;
+  a.mode = 0;
+  a.scale = d.scale;
+  a.c = nullptr;
+  a.o = d.o;
+  a.out_f32 = d.out_f32;
+  a.unnormalized = 0;
+  a.lse = d.lse;
+  a.err = d.err;
+  TcParams P;
+  init_common(P, a);
+  P.seg = 1;
+  P.W = d.W;
+  P.I = d.I;
+  P.part_rank = d.part_rank;
+  P.nsteps = d.part_rank >= 0 ? 2 : 2 * d.W;
+  if (P.units == 0) return cudaSuccess;
+  TcMaps maps;
+  if (!encode_bf16_2d_sw128(&maps.q, d.q, (uint64_t)d.Hq * d.Sc, kD, kBM, 64))
+    return cudaErrorInvalidValue;
+  for (int r = 0; r < d.W; ++r) {
+    P.lp[r] = dcp_local_filled(d.P, d.W, d.I, d.I, r);
+    P.lc[r] = dcp_local_filled(d.Sc, d.W, d.I, d.I, r);
+    if (P.lp[r] > d.Lcap) P.lp[r] = d.Lcap;
+    if (P.lc[r] > d.Lc) P.lc[r] = d.Lc;
+    const uint64_t rp = P.lp[r] > 0 ? (uint64_t)P.lp[r] : 1, rc = P.lc[r] > 0 ? (uint64_t)P.lc[r] : 1;
+    const char* kp = (const char*)d.k_prior + (size_t)r * d.Hkv * d.Lcap * d.D * 2;
+    const char* vp = (const char*)d.v_prior + (size_t)r * d.Hkv * d.Lcap * d.D * 2;
+    const char* kc = (const char*)d.k_cur + (size_t)r * d.Hkv * d.Lc * d.D * 2;
+    const char* vc = (const char*)d.v_cur + (size_t)r * d.Hkv * d.Lc * d.D * 2;
+    if (!encode_bf16_3d_sw128(&maps.kv[4 * r + 0], kp, d.Hkv, rp, kD, (uint64_t)d.Lcap * kD, kBN, 64) ||
+        !encode_bf16_3d_sw128(&maps.kv[4 * r + 1], vp, d.Hkv, rp, kD, (uint64_t)d.Lcap * kD, kBN, 64) ||
+        !encode_bf16_3d_sw128(&maps.kv[4 * r + 2], kc, d.Hkv, rc, kD, (uint64_t)d.Lc * kD, kBN, 64) ||
+        !encode_bf16_3d_sw128(&maps.kv[4 * r + 3], vc, d.Hkv, rc, kD, (uint64_t)d.Lc * kD, kBN, 64))
+      return cudaErrorInvalidValue;
+  }
+  return launch_tc(maps, P, stream);
 }
 
 }  // namespace ca

@@ -39,4 +39,24 @@ inline bool encode_bf16_2d_sw128(CUtensorMap* map, const void* base, uint64_t ro
   return r == CUDA_SUCCESS;
 }
 
+// 3-D bf16 tensor map over `depth` matrices of [rows, cols] (row stride
+// cols elements, matrix stride `mat_stride_elems`), box [1, box_rows,
+// box_cols], 128-byte swizzle.  Rows >= `rows` read as zero, which is how a
+// caller masks the unused tail of a cache or shard.
+inline bool encode_bf16_3d_sw128(CUtensorMap* map, const void* base, uint64_t depth,
+                                 uint64_t rows, uint64_t cols, uint64_t mat_stride_elems,
+                                 uint32_t box_rows, uint32_t box_cols) {
+  auto fn = get_encode_tiled();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cols, rows, depth};
+  cuuint64_t strides[2] = {cols * 2, mat_stride_elems * 2};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace ca

@@ -86,3 +86,15 @@ def decode_inputs(N, Hq, Hkv, D, W, Lloc, seed, dtype=torch.bfloat16, device="cp
         for r in range(W):
             t[r].copy_(torch.randn(N, Hkv, Lloc, D, generator=g, device=device).to(dtype))
     return q, k, v
+
+
+def dcp_prefill_inputs(Hq, Hkv, D, W, Sc, Lcap, Lc, seed, dtype=torch.bfloat16, device="cpu"):
+    """q [Hq,Sc,D], prior shards [W,Hkv,Lcap,D] and current-chunk shards
+    [W,Hkv,Lc,D], all N(0,1)."""
+    g = _gen(seed, device)
+    q = torch.randn(Hq, Sc, D, generator=g, device=device).to(dtype)
+    kp = torch.randn(W, Hkv, Lcap, D, generator=g, device=device).to(dtype)
+    vp = torch.randn(W, Hkv, Lcap, D, generator=g, device=device).to(dtype)
+    kc = torch.randn(W, Hkv, Lc, D, generator=g, device=device).to(dtype)
+    vc = torch.randn(W, Hkv, Lc, D, generator=g, device=device).to(dtype)
+    return q, kp, vp, kc, vc

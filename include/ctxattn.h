@@ -230,6 +230,45 @@ ca_status ca_dcp_decode_noalloc(const void *q, const void *k_shards,
                                 void *stream);
 
 /* ------------------------------------------------------------------------
+ * DCP prefill of one chunk ([DCP] "Segmented Attention CP", "DCP Prefill"
+ * compute pattern): the chunk's Sc gathered queries (global positions
+ * P .. P+Sc-1, P = prior_tokens) attend, on every rank R, to R's local KV --
+ * its prior cache slots (the positions [0, P) it was dealt, slot s at global
+ * (s/I)*(dcp*I) + R*I + s%I) and its share of the chunk (chunk position p
+ * dealt from the chunk start, global P + p) -- with a causal mask on global
+ * positions; the per-rank partials (o_R, lse_R) are LSE-merged.  On one GPU
+ * the merge happens in the accumulator; ca_dcp_prefill_partial returns one
+ * rank's partial for an explicit ca_lse_merge.  Online max only.
+ *
+ * q           device [Hq, Sc, D] bf16.
+ * k_prior, v_prior  device [dcp, Hkv, Lcap, D] bf16; rank R's prior slot s
+ *             in row s; slots >= local_filled(P, R) are never read (any
+ *             values, NaN included).
+ * k_cur, v_cur device [dcp, Hkv, Lc, D] bf16; rank R's chunk token j in row
+ *             j; rows >= local_filled(Sc, R) are never read.
+ * o           device [Hq, Sc, D] bf16 (ca_dcp_prefill) or fp32
+ *             (ca_dcp_prefill_partial: the normalised partial of `rank`).
+ * lse         device [Hq, Sc] fp32 (nullable for ca_dcp_prefill).
+ * Errors: CA_ERR_SHAPE if Hq % Hkv != 0, Lcap < local_filled(P, 0) or
+ * Lc < local_filled(Sc, 0); CA_ERR_UNSUPPORTED unless bf16 with D = 128 and
+ * 1 <= dcp <= 8.
+ * ---------------------------------------------------------------------- */
+ca_status ca_dcp_prefill(const void *q, const void *k_prior, const void *v_prior,
+                         const void *k_cur, const void *v_cur, ca_dtype dtype,
+                         int Hq, int Hkv, int64_t Sc, int D, int dcp,
+                         int interleave, int64_t prior_tokens, int64_t Lcap,
+                         int64_t Lc, float softmax_scale, void *o, float *lse,
+                         void *stream);
+ca_status ca_dcp_prefill_partial(const void *q, const void *k_prior,
+                                 const void *v_prior, const void *k_cur,
+                                 const void *v_cur, ca_dtype dtype, int Hq,
+                                 int Hkv, int64_t Sc, int D, int dcp,
+                                 int interleave, int64_t prior_tokens,
+                                 int64_t Lcap, int64_t Lc, int rank,
+                                 float softmax_scale, float *o_part,
+                                 float *lse_part, void *stream);
+
+/* ------------------------------------------------------------------------
  * Device layout permutations (bit-exact copies of rows of row_bytes bytes).
  *
  * ca_layout_to_shards: x holds BH heads of S rows in global token order;

@@ -66,7 +66,7 @@ def _load():
             lib.ora_dcp_local_filled.argtypes = [I64, I, I, I]
             lib.ora_dcp_local_filled.restype = I64
             lib.ora_dcp_decode.argtypes = [P, P, P, I, I, I, I64, I, I, I, P, Dbl, P, P]
-            lib.ora_dcp_prefill.argtypes = [P, P, P, P, P, I, I, I64, I, I, I, I64, I64, I64, Dbl, I, P, P]
+            lib.ora_dcp_prefill.argtypes = [P, P, P, P, P, I, I, I64, I, I, I, I64, I64, I64, Dbl, I, P, I64, P, P]
             lib.ora_num_threads.restype = I
             _lib = lib
     return _lib
@@ -208,19 +208,24 @@ def dcp_decode(q, k_shards, v_shards, interleave, seq_lens=None, scale=None):
     return o, lse
 
 
-def dcp_prefill(q, k_prior, v_prior, k_cur, v_cur, interleave, prior_tokens, scale=None, part_rank=-1):
+def dcp_prefill(q, k_prior, v_prior, k_cur, v_cur, interleave, prior_tokens, scale=None, part_rank=-1,
+                rows=None):
     """DCP prefill of one chunk.  q [Hq,Sc,D]; prior shards [W,Hkv,Lcap,D];
     current shards [W,Hkv,Lc,D].  Returns (o [Hq,Sc,D], lse [Hq,Sc]); with
-    part_rank >= 0 returns that rank's partial instead of the merge."""
+    part_rank >= 0 returns that rank's partial instead of the merge.  With
+    ``rows`` (flat ids h*Sc + i) returns only those rows: (o [n,D], lse [n])."""
     q = _f32(q)
     k_prior, v_prior, k_cur, v_cur = _f32(k_prior), _f32(v_prior), _f32(k_cur), _f32(v_cur)
     Hq, Sc, D = q.shape
     W, Hkv, Lcap, _ = k_prior.shape
     Lc = k_cur.shape[2]
     scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
-    o = np.zeros((Hq, Sc, D))
-    lse = np.zeros((Hq, Sc))
+    r = np.arange(Hq * Sc, dtype=np.int64) if rows is None else np.ascontiguousarray(np.asarray(rows, np.int64))
+    o = np.zeros((len(r), D))
+    lse = np.zeros(len(r))
     _load().ora_dcp_prefill(_ptr(q), _ptr(k_prior), _ptr(v_prior), _ptr(k_cur), _ptr(v_cur), Hq, Hkv, Sc, D,
-                            W, int(interleave), int(prior_tokens), Lcap, Lc, scale, int(part_rank), _ptr(o),
-                            _ptr(lse))
+                            W, int(interleave), int(prior_tokens), Lcap, Lc, scale, int(part_rank), _ptr(r), len(r),
+                            _ptr(o), _ptr(lse))
+    if rows is None:
+        return o.reshape(Hq, Sc, D), lse.reshape(Hq, Sc)
     return o, lse

@@ -415,13 +415,14 @@ void ora_dcp_decode(const float *q, const float *k_shards,
  *
  * q [Hq, Sc, D]; k_prior, v_prior [W, Hkv, Lcap, D] (slot s of rank R in
  * row s); k_cur, v_cur [W, Hkv, Lc, D] (current token j of rank R in row j).
- * o [Hq, Sc, D], lse [Hq, Sc].  If part_rank >= 0 only that rank's partial
- * is computed (no merge). */
+ * rows: flat query ids h*Sc + i to compute (nrows of them); o [nrows, D],
+ * lse [nrows].  If part_rank >= 0 only that rank's partial is computed (no
+ * merge). */
 void ora_dcp_prefill(const float *q, const float *k_prior, const float *v_prior,
                      const float *k_cur, const float *v_cur, int Hq, int Hkv,
                      int64_t Sc, int D, int W, int I, int64_t P, int64_t Lcap,
-                     int64_t Lc, double scale, int part_rank, double *o,
-                     double *lse) {
+                     int64_t Lc, double scale, int part_rank, const int64_t *rows,
+                     int64_t nrows, double *o, double *lse) {
   int G = Hq / Hkv;
   int32_t *own_p = (int32_t *)malloc(sizeof(int32_t) * (size_t)(P > 0 ? P : 1));
   int64_t *loc_p = (int64_t *)malloc(sizeof(int64_t) * (size_t)(P > 0 ? P : 1));
@@ -430,7 +431,8 @@ void ora_dcp_prefill(const float *q, const float *k_prior, const float *v_prior,
   ora_dcp_deal(P, W, I, own_p, loc_p);
   ora_dcp_deal(Sc, W, I, own_c, loc_c);
 #pragma omp parallel for schedule(dynamic, 1)
-  for (int64_t hi = 0; hi < (int64_t)Hq * Sc; ++hi) {
+  for (int64_t ri = 0; ri < nrows; ++ri) {
+    const int64_t hi = rows[ri];
     int64_t h = hi / Sc, i = hi % Sc, hk = h / G;
     const float *qrow = q + hi * D;
     double *op = (double *)calloc((size_t)W * D, sizeof(double));
@@ -477,10 +479,10 @@ void ora_dcp_prefill(const float *q, const float *k_prior, const float *v_prior,
       }
     }
     if (part_rank >= 0) {
-      for (int d = 0; d < D; ++d) o[hi * D + d] = op[(int64_t)part_rank * D + d];
-      lse[hi] = lp[part_rank];
+      for (int d = 0; d < D; ++d) o[ri * D + d] = op[(int64_t)part_rank * D + d];
+      lse[ri] = lp[part_rank];
     } else {
-      ora_lse_merge(op, lp, W, 1, D, o + hi * D, lse + hi);
+      ora_lse_merge(op, lp, W, 1, D, o + ri * D, lse + ri);
     }
     free(op);
     free(lp);

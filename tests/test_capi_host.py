@@ -118,3 +118,27 @@ def test_merge_bound_decode_layout_validation(ca):
     assert S[lib.ca_layout_to_shards(FAKE, FAKE, 2, 100, 256, 8, 0, None)] == "CA_ERR_SHAPE"
     assert S[lib.ca_layout_to_shards(FAKE, FAKE, 2, 64, 100, 8, 0, None)] == "CA_ERR_UNSUPPORTED"
     assert S[lib.ca_dcp_shard_kv(FAKE, FAKE, 2, 100, 256, 4, 16, None)] == "CA_ERR_SHAPE"
+
+
+def test_dcp_prefill_validation(ca):
+    lib = ca._load()
+    S = ca.STATUS
+
+    def pre(**kw):
+        a = dict(q=FAKE, kp=FAKE, vp=FAKE, kc=FAKE, vc=FAKE, dtype=1, Hq=8, Hkv=2, Sc=512, D=128, W=4, I=16,
+                 P=1024, Lcap=256, Lc=128, scale=0.0, o=FAKE, lse=None, stream=None)
+        a.update(kw)
+        return lib.ca_dcp_prefill(a["q"], a["kp"], a["vp"], a["kc"], a["vc"], a["dtype"], a["Hq"], a["Hkv"], a["Sc"],
+                                  a["D"], a["W"], a["I"], a["P"], a["Lcap"], a["Lc"], a["scale"], a["o"], a["lse"],
+                                  a["stream"])
+
+    assert S[pre(q=None)] == "CA_ERR_INVALID_ARG"
+    assert S[pre(P=-1)] == "CA_ERR_INVALID_ARG"
+    assert S[pre(Hq=6, Hkv=4)] == "CA_ERR_SHAPE"
+    assert S[pre(Lcap=255)] == "CA_ERR_SHAPE"   # rank 0 holds 256 of 1024 prior tokens
+    assert S[pre(Lc=127)] == "CA_ERR_SHAPE"     # and 128 of the 512-token chunk
+    assert S[pre(W=9)] == "CA_ERR_UNSUPPORTED"
+    assert S[pre(dtype=0)] == "CA_ERR_UNSUPPORTED"
+    assert S[pre(kc=FAKE + 8)] == "CA_ERR_ALIGNMENT"
+    assert S[lib.ca_dcp_prefill_partial(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 512, 128, 4, 16, 1024, 256, 128, 4,
+                                        0.0, FAKE, FAKE, None)] == "CA_ERR_INVALID_ARG"  # rank out of range
