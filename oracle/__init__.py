@@ -67,6 +67,7 @@ def _load():
             lib.ora_dcp_local_filled.restype = I64
             lib.ora_dcp_decode.argtypes = [P, P, P, I, I, I, I64, I, I, I, P, Dbl, P, P]
             lib.ora_dcp_prefill.argtypes = [P, P, P, P, P, I, I, I64, I, I, I, I64, I64, I64, Dbl, I, P, I64, P, P]
+            lib.ora_dcp_decode_paged.argtypes = [P, P, P, P, I, I, I, I64, I, I64, I, I, I, P, Dbl, P, P]
             lib.ora_num_threads.restype = I
             _lib = lib
     return _lib
@@ -228,4 +229,22 @@ def dcp_prefill(q, k_prior, v_prior, k_cur, v_cur, interleave, prior_tokens, sca
                             _ptr(o), _ptr(lse))
     if rows is None:
         return o.reshape(Hq, Sc, D), lse.reshape(Hq, Sc)
+    return o, lse
+
+
+def dcp_decode_paged(q, k_cache, v_cache, block_tables, interleave, seq_lens, scale=None):
+    """DCP decode over paged caches.  q [N,Hq,D]; k/v cache [W,nblk,Hkv,bs,D];
+    block_tables [W,N,max_blocks] int32; seq_lens [N].  Returns (o, lse)."""
+    q = _f32(q)
+    k_cache, v_cache = _f32(k_cache), _f32(v_cache)
+    bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    N, Hq, D = q.shape
+    W, nblk, Hkv, bs, _ = k_cache.shape
+    max_blocks = bt.shape[2]
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int64))
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    o = np.zeros((N, Hq, D))
+    lse = np.zeros((N, Hq))
+    _load().ora_dcp_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), N, Hq, Hkv, nblk, bs, max_blocks,
+                                 D, W, int(interleave), _ptr(sl), scale, _ptr(o), _ptr(lse))
     return o, lse

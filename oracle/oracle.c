@@ -493,6 +493,47 @@ void ora_dcp_prefill(const float *q, const float *k_prior, const float *v_prior,
   free(loc_c);
 }
 
+/* DCP decode over a paged KV cache ("DCP (Decode Context Parallelism)",
+ * sections "Slot Mapping and KV Cache" and "Segmented Attention CP", step 1:
+ * the prior KV is read from the cache through the block table).  Rank r's
+ * cache holds blocks of `bs` slots per KV head: k_cache[r][blk][hk][t][d]
+ * ([W, nblk, Hkv, bs, D]).  Local slot s of sequence n on rank r lives in
+ * block block_tables[r][n][s / bs] at offset s % bs.  The decode itself is
+ * ora_dcp_decode's: gather each rank's local slots in order, then the same
+ * per-rank partials and LSE merge.  block_tables is [W, N, max_blocks]. */
+void ora_dcp_decode_paged(const float *q, const float *k_cache, const float *v_cache,
+                          const int32_t *block_tables, int N, int Hq, int Hkv, int64_t nblk,
+                          int bs, int64_t max_blocks, int D, int W, int I,
+                          const int64_t *seq_lens, double scale, double *o, double *lse) {
+  int64_t Lloc = max_blocks * bs;
+  float *ks = (float *)calloc((size_t)W * N * Hkv * Lloc * D, sizeof(float));
+  float *vs = (float *)calloc((size_t)W * N * Hkv * Lloc * D, sizeof(float));
+  for (int r = 0; r < W; ++r)
+    for (int n = 0; n < N; ++n) {
+      /* only the slots the sequence actually has on this rank are gathered */
+      int32_t *own = (int32_t *)malloc(sizeof(int32_t) * (size_t)(seq_lens[n] > 0 ? seq_lens[n] : 1));
+      int64_t *loc = (int64_t *)malloc(sizeof(int64_t) * (size_t)(seq_lens[n] > 0 ? seq_lens[n] : 1));
+      ora_dcp_deal(seq_lens[n], W, I, own, loc);
+      for (int64_t p = 0; p < seq_lens[n]; ++p) {
+        if (own[p] != r) continue;
+        int64_t s = loc[p];
+        int64_t blk = block_tables[((int64_t)r * N + n) * max_blocks + s / bs];
+        for (int hk = 0; hk < Hkv; ++hk)
+          for (int d = 0; d < D; ++d) {
+            int64_t src = (((int64_t)r * nblk + blk) * Hkv + hk) * bs * D + (s % bs) * D + d;
+            int64_t dst = ((((int64_t)r * N + n) * Hkv + hk) * Lloc + s) * D + d;
+            ks[dst] = k_cache[src];
+            vs[dst] = v_cache[src];
+          }
+      }
+      free(own);
+      free(loc);
+    }
+  ora_dcp_decode(q, ks, vs, N, Hq, Hkv, Lloc, D, W, I, seq_lens, scale, o, lse);
+  free(ks);
+  free(vs);
+}
+
 /* Number of OpenMP threads a parallel region here would use. */
 int ora_num_threads(void) {
 #ifdef _OPENMP

@@ -402,3 +402,34 @@ def test_dcp_prefill_zero_query_prefix_means():
     for i in range(Sc):
         np.testing.assert_allclose(o[:, i], np.broadcast_to(vg[0, : P + i + 1].astype(np.float64).mean(0), (Hq, D)), atol=1e-12)
         np.testing.assert_allclose(lse[:, i], math.log(P + i + 1), atol=1e-12)
+
+
+# ---------------------------------------------------------------- paged DCP decode
+
+
+def test_dcp_decode_paged_equals_contiguous_shards():
+    """Scattering each rank's local slots over shuffled physical blocks of a
+    paged cache (block table per rank and sequence) changes nothing: the
+    paged decode equals the decode over the contiguous shards."""
+    N, Hq, Hkv, D, W, I, bs = 3, 4, 2, 8, 4, 16, 16
+    Lloc = 64
+    max_blocks = Lloc // bs
+    q = rnd(N, Hq, D)
+    ks, vs = rnd(W, N, Hkv, Lloc, D), rnd(W, N, Hkv, Lloc, D)
+    seq_lens = np.array([W * Lloc, 100, 1])
+    nblk = N * max_blocks + 5
+    kc = rnd(W, nblk, Hkv, bs, D) * 100  # unused blocks: junk
+    vc = rnd(W, nblk, Hkv, bs, D) * 100
+    bt = np.zeros((W, N, max_blocks), np.int32)
+    rng = np.random.default_rng(5)
+    for r in range(W):
+        perm = rng.permutation(nblk)[: N * max_blocks].reshape(N, max_blocks)
+        bt[r] = perm
+        for n in range(N):
+            for lb in range(max_blocks):
+                kc[r, perm[n, lb]] = ks[r, n, :, lb * bs:(lb + 1) * bs]
+                vc[r, perm[n, lb]] = vs[r, n, :, lb * bs:(lb + 1) * bs]
+    o1, l1 = ora.dcp_decode(q, ks, vs, I, seq_lens=seq_lens)
+    o2, l2 = ora.dcp_decode_paged(q, kc, vc, bt, I, seq_lens)
+    np.testing.assert_allclose(o2, o1, atol=1e-12)
+    np.testing.assert_allclose(l2, l1, atol=1e-12)
