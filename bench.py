@@ -415,6 +415,39 @@ def bench_other_workloads(ca, torch, reps=5):
                                                                "tflops": round(f / (ms / 1e3) / 1e12, 1)}
     del q, kp, vp, kc, vc
     torch.cuda.empty_cache()
+    # paged DCP decode: the decode workload's 34 GB of K/V in 16-slot blocks
+    # scattered over each rank's cache by a random block table
+    d = DECODE
+    bs = 16
+    mb = d["Lloc"] // bs
+    nblk = d["N"] * mb
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    q = torch.randn(d["N"], d["Hq"], d["D"], generator=g, device="cuda").to(torch.bfloat16)
+    kc = torch.empty(d["W"], nblk, d["Hkv"], bs, d["D"], device="cuda", dtype=torch.bfloat16)
+    vc = torch.empty_like(kc)
+    for t in (kc, vc):
+        for r in range(d["W"]):
+            t[r].copy_(torch.randn(nblk, d["Hkv"], bs, d["D"], generator=g, device="cuda").to(torch.bfloat16))
+    bt = torch.stack([torch.randperm(nblk, generator=g, device="cuda").view(d["N"], mb)
+                      for _ in range(d["W"])]).to(torch.int32).contiguous()
+    sl = torch.full((d["N"],), d["W"] * d["Lloc"], dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty(d["N"], d["Hq"], device="cuda", dtype=torch.float32)
+    ws = torch.empty(ca.dcp_decode_workspace_size(d["N"], d["Hq"], d["Hkv"], d["Lloc"], d["D"], d["W"], d["I"]),
+                     dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        ca.dcp_decode_paged(q, kc, vc, bt, d["I"], sl, out=out, lse=lse, workspace=ws)
+    a.record(stream)
+    for _ in range(reps):
+        ca.dcp_decode_paged(q, kc, vc, bt, d["I"], sl, out=out, lse=lse, workspace=ws)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    res["dcp_decode_paged bs16 64seqs L131072 dcp4"] = {"ms": round(ms, 3),
+                                                        "gbs": round(decode_bytes() / (ms / 1e3) / 1e9, 1)}
+    del q, kc, vc, bt
+    torch.cuda.empty_cache()
     return res
 
 

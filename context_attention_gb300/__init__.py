@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "CtxAttnError", "build", "library_path", "ring_attn_fwd", "ring_attn_fwd_bounded", "attn_partial_step", "lse_merge",
-    "const_max_bound", "dcp_decode", "dcp_decode_noalloc", "dcp_prefill", "dcp_prefill_partial", "layout_to_shards", "layout_from_shards", "dcp_shard_kv",
+    "const_max_bound", "dcp_decode", "dcp_decode_noalloc", "dcp_decode_paged", "paged_kv_write", "dcp_prefill", "dcp_prefill_partial", "layout_to_shards", "layout_from_shards", "dcp_shard_kv",
     "layout_global_index", "layout_shard_row", "ring_kv_shard", "dcp_owner", "dcp_local_index",
     "dcp_local_to_global", "dcp_local_filled", "dcp_active_mask", "dcp_slot_mapping",
     "device_status", "ring_attn_fwd_workspace_size", "dcp_decode_workspace_size",
@@ -78,6 +78,8 @@ def _load():
             "ca_dcp_decode_workspace_size": ([I, I, I, I64, I, I, I], SZ),
             "ca_dcp_decode": ([P, P, P, I, I, I, I, I64, I, I, I, P, F, P, P, P, SZ, P], I),
             "ca_dcp_decode_noalloc": ([P, P, P, I, I, I, I, I64, I, I, I, P, F, P, P, P], I),
+            "ca_dcp_decode_paged": ([P, P, P, P, I, I, I, I, I64, I, I64, I, I, I, P, F, P, P, P, SZ, P], I),
+            "ca_paged_kv_write": ([P, P, P, P, P, I, I, I, I, I, I64, I, P], I),
             "ca_dcp_prefill": ([P, P, P, P, P, I, I, I, I64, I, I, I, I64, I64, I64, F, P, P, P], I),
             "ca_dcp_prefill_partial": ([P, P, P, P, P, I, I, I, I64, I, I, I, I64, I64, I64, I, F, P, P, P], I),
             "ca_layout_to_shards": ([P, P, I64, I64, I64, I, I, P], I),
@@ -287,6 +289,47 @@ def dcp_decode_noalloc(q, k_shards, v_shards, interleave, seq_lens=None, softmax
                                    _ptr(lse), _stream(q))
     _check("ca_dcp_decode_noalloc", st)
     return out, lse
+
+
+def dcp_decode_paged(q, k_cache, v_cache, block_tables, interleave, seq_lens, softmax_scale=None, out=None,
+                     lse=None, workspace=None):
+    """DCP decode over paged caches.  q [N,Hq,D]; k/v cache [dcp,nblk,Hkv,bs,D];
+    block_tables CUDA int32 [dcp,N,max_blocks]; seq_lens CUDA int32 [N]."""
+    lib = _load()
+    _need(q, "q", 3)
+    _need(k_cache, "k_cache", 5)
+    _need(v_cache, "v_cache", 5)
+    N, Hq, D = q.shape
+    W, nblk, Hkv, bs, _ = k_cache.shape
+    max_blocks = block_tables.shape[2]
+    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens)):
+        if not (t.is_cuda and t.dtype == torch.int32 and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA int32 tensor")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(N, Hq, device=q.device, dtype=torch.float32)
+    ws_bytes = int(lib.ca_dcp_decode_workspace_size(N, Hq, Hkv, max_blocks * bs, D, W, interleave))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), device=q.device, dtype=torch.uint8)
+    st = lib.ca_dcp_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), DTYPE[q.dtype], N, Hq,
+                                 Hkv, nblk, bs, max_blocks, D, W, interleave, _ptr(seq_lens),
+                                 float(softmax_scale or 0.0), _ptr(out), _ptr(lse), _ptr(workspace),
+                                 workspace.numel(), _stream(q))
+    _check("ca_dcp_decode_paged", st)
+    return out, lse
+
+
+def paged_kv_write(k_new, v_new, slots, k_cache, v_cache):
+    """Write new tokens' K/V [T,Hkv,D] into the paged caches by slot mapping
+    (slots: CUDA int64 [dcp, T], -1 = not owned)."""
+    T, Hkv, D = k_new.shape
+    W, nblk, _, bs, _ = k_cache.shape
+    if not (slots.is_cuda and slots.dtype == torch.int64 and slots.is_contiguous()):
+        raise ValueError("slots must be a contiguous CUDA int64 tensor")
+    st = _load().ca_paged_kv_write(_ptr(k_new), _ptr(v_new), _ptr(slots), _ptr(k_cache), _ptr(v_cache),
+                                   DTYPE[k_new.dtype], T, Hkv, D, W, nblk, bs, _stream(k_new))
+    _check("ca_paged_kv_write", st)
 
 
 def dcp_prefill(q, k_prior, v_prior, k_cur, v_cur, interleave, prior_tokens, softmax_scale=None, out=None,

@@ -330,11 +330,88 @@ ca_status ca_dcp_decode(const void* q, const void* k_shards, const void* v_shard
   a.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                          align256(sizeof(float) * parts * N * Hq * D));
   a.err = err;
+  a.paged = 0;
+  a.block_tables = nullptr;
+  a.nblk = a.max_blocks = 0;
+  a.bs = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_dcp_decode_partials(a, s);
   if (e != cudaSuccess) return launched(e);
   return launched(launch_lse_merge(a.o_parts, a.lse_parts, (int)parts, (int64_t)N * Hq, D, nullptr,
                                    o, 1, lse, s));
+}
+
+ca_status ca_dcp_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, ca_dtype dtype, int N, int Hq, int Hkv,
+                              int64_t nblk, int block_size, int64_t max_blocks, int D, int dcp,
+                              int interleave, const int32_t* seq_lens, float softmax_scale, void* o,
+                              float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !o) return CA_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || N <= 0 || Hq <= 0 || Hkv <= 0 || nblk <= 0 || block_size <= 0 ||
+      max_blocks <= 0 || D <= 0 || dcp <= 0 || interleave <= 0)
+    return CA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return CA_ERR_SHAPE;
+  if (dtype != CA_DTYPE_BF16 || D != 128 || Hq / Hkv > 8) return CA_ERR_UNSUPPORTED;
+  if (block_size != 8 && block_size != 16 && block_size != 32 && block_size != 64 &&
+      block_size != 128)
+    return CA_ERR_UNSUPPORTED;
+  if ((int64_t)dcp * nblk * Hkv * block_size >= ((int64_t)1 << 31)) return CA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return CA_ERR_ALIGNMENT;
+  const int64_t Lloc = max_blocks * block_size;
+  const size_t need = ca_dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, dcp, interleave);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return CA_ERR_WORKSPACE;
+  ca_status st = device_is_gb300();
+  if (st != CA_OK) return st;
+  unsigned* err = device_error_word();
+  if (!err) return CA_ERR_CUDA;
+  DecodeArgs a;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.N = N;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.W = dcp;
+  a.I = interleave;
+  a.Lloc = Lloc;
+  a.seq_lens = seq_lens;
+  a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
+  dcp_decode_split(Lloc, &a.chunk, &a.splits);
+  const size_t parts = (size_t)dcp * a.splits;
+  a.o_parts = static_cast<float*>(workspace);
+  a.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         align256(sizeof(float) * parts * N * Hq * D));
+  a.err = err;
+  a.paged = 1;
+  a.block_tables = block_tables;
+  a.nblk = nblk;
+  a.max_blocks = max_blocks;
+  a.bs = block_size;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_dcp_decode_partials(a, s);
+  if (e != cudaSuccess) return launched(e);
+  return launched(launch_lse_merge(a.o_parts, a.lse_parts, (int)parts, (int64_t)N * Hq, D, nullptr,
+                                   o, 1, lse, s));
+}
+
+ca_status ca_paged_kv_write(const void* k_new, const void* v_new, const int64_t* slots,
+                            void* k_cache, void* v_cache, ca_dtype dtype, int T, int Hkv, int D,
+                            int dcp, int64_t nblk, int block_size, void* stream) {
+  if (!k_new || !v_new || !slots || !k_cache || !v_cache) return CA_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || T < 0 || Hkv <= 0 || D <= 0 || dcp <= 0 || nblk <= 0 ||
+      block_size <= 0)
+    return CA_ERR_INVALID_ARG;
+  const int elem = dtype == CA_DTYPE_BF16 ? 2 : 4;
+  if ((D * elem) % 16 != 0) return CA_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slots) & 7u))
+    return CA_ERR_ALIGNMENT;
+  return launched(launch_paged_kv_write(k_new, v_new, slots, k_cache, v_cache, T, Hkv, D, dcp, nblk,
+                                        block_size, elem, static_cast<cudaStream_t>(stream)));
 }
 
 // ------------------------------------------------------------------ DCP prefill

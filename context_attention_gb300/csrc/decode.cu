@@ -114,6 +114,7 @@ __device__ __forceinline__ uint32_t sw128(int tok, int chunk) {
   return (uint32_t)(tok * 128 + ((chunk ^ (tok & 7)) << 4));
 }
 
+template <bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
 dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                   const DecParams P) {
@@ -142,7 +143,49 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
   }
   __syncthreads();
 
-  if (warp == kProducerWarp) {
+  if (warp == kProducerWarp && kPaged) {
+    // Paged cache: a stage's 128 slots are up to 128/bs blocks scattered over
+    // the cache.  Lane i fetches block i of the stage through the block table
+    // and loads it as bs-row boxes at row offset i*bs of the stage; a box
+    // written at a 1024-byte-aligned offset has the same 128B swizzle as the
+    // rows of one 128-row box, so the consumers read the stage unchanged.
+    const uint64_t policy = l2_policy_evict_first();
+    const uint32_t box_bytes = (uint32_t)a.bs * 128;
+    uint64_t pos = 0;
+    bool ok = true;
+    for (int64_t it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
+      const Item I = item_of(P, it);
+      const int nst = (int)((I.ntok + kTok - 1) / kTok);
+      const int32_t* bt = a.block_tables + ((int64_t)I.r * a.N + I.n) * a.max_blocks;
+      for (int st = 0; st < nst; ++st) {
+        const int slot = (int)(pos % kStages);
+        ok = __all_sync(0xffffffffu, mbar_wait(empty(slot), (uint32_t)(((pos / kStages) & 1) ^ 1),
+                                               abort_flag, err));
+        if (!ok) break;
+        const int64_t first = I.t0 + (int64_t)st * kTok;  // first local slot of the stage
+        const int64_t nvalid = min((int64_t)kTok, I.ntok - (int64_t)st * kTok);
+        const int nb = (int)((nvalid + a.bs - 1) / a.bs);
+        if (lane == 0) mbar_arrive_expect_tx(full(slot), (uint32_t)nb * 4 * box_bytes);
+        __syncwarp();
+        if (lane < nb) {
+          const int64_t blk = bt[first / a.bs + lane];
+          const int row = (int)((((int64_t)I.r * a.nblk + blk) * a.Hkv + I.hkv) * a.bs);
+          const uint32_t dst = sbase + kSmemStages + slot * kStageBytes + (uint32_t)lane * box_bytes;
+          tma_load_2d_hint(dst + 0 * kBox, &tk, full(slot), 0, row, policy);
+          tma_load_2d_hint(dst + 1 * kBox, &tk, full(slot), 64, row, policy);
+          tma_load_2d_hint(dst + 2 * kBox, &tv, full(slot), 0, row, policy);
+          tma_load_2d_hint(dst + 3 * kBox, &tv, full(slot), 64, row, policy);
+        }
+        ++pos;
+      }
+    }
+    if (!ok && lane == 0) {
+      for (uint64_t p = pos > kStages ? pos - kStages : 0; p < pos; ++p) {
+        volatile int never = 0;
+        mbar_wait(full((int)(p % kStages)), (uint32_t)((p / kStages) & 1), &never, err);
+      }
+    }
+  } else if (warp == kProducerWarp) {
     if (lane == 0) {
       prefetch_tensormap(&tk);
       prefetch_tensormap(&tv);
@@ -369,6 +412,24 @@ void dcp_decode_split(int64_t Lloc, int64_t* chunk, int* splits) {
   if (*splits < 1) *splits = 1;
 }
 
+template <bool kPaged>
+static cudaError_t launch_decode(const DecParams& P, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 cudaStream_t stream) {
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(dcp_decode_kernel<kPaged>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  const int sms = device_sm_count();
+  const int64_t grid = P.items < sms ? P.items : sms;
+  dcp_decode_kernel<kPaged><<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(tk, tv, P);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dcp_decode_partials(const DecodeArgs& a, cudaStream_t stream) {
   DecParams P;
   P.a = a;
@@ -377,22 +438,58 @@ cudaError_t launch_dcp_decode_partials(const DecodeArgs& a, cudaStream_t stream)
   P.scale_log2 = a.scale * kLog2e;
   if (P.items == 0) return cudaSuccess;
   CUtensorMap tk, tv;
+  if (a.paged) {
+    const uint64_t rows = (uint64_t)a.W * a.nblk * a.Hkv * a.bs;
+    if (!encode_bf16_2d_sw128(&tk, a.k, rows, kD, (uint32_t)a.bs, 64) ||
+        !encode_bf16_2d_sw128(&tv, a.v, rows, kD, (uint32_t)a.bs, 64))
+      return cudaErrorInvalidValue;
+    return launch_decode<true>(P, tk, tv, stream);
+  }
   const uint64_t rows = (uint64_t)a.W * a.N * a.Hkv * a.Lloc;
   if (!encode_bf16_2d_sw128(&tk, a.k, rows, kD, kTok, 64) ||
       !encode_bf16_2d_sw128(&tv, a.v, rows, kD, kTok, 64))
     return cudaErrorInvalidValue;
-  static int attr_set[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(dcp_decode_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = 1;
+  return launch_decode<false>(P, tk, tv, stream);
+}
+
+// Slot-mapping write of new tokens' K/V into the paged caches: token t goes
+// to rank r's slot slots[r*T + t] (block slot / bs, offset slot % bs) unless
+// that slot is -1 (the rank does not own the token).  Bit-exact copies of
+// 16-byte chunks; one thread per chunk.
+__global__ void __launch_bounds__(256)
+paged_kv_write_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                      const int64_t* __restrict__ slots, uint4* __restrict__ k_cache,
+                      uint4* __restrict__ v_cache, int T, int Hkv, int chunks, int W, int64_t nblk,
+                      int bs) {
+  const int64_t total = (int64_t)W * T * Hkv * chunks;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % chunks);
+    const int h = (int)((i / chunks) % Hkv);
+    const int64_t rt = i / ((int64_t)chunks * Hkv);  // r*T + t
+    const int t = (int)(rt % T);
+    const int r = (int)(rt / T);
+    const int64_t slot = slots[rt];
+    if (slot < 0 || slot / bs >= nblk) continue;
+    const int64_t dst = ((((int64_t)r * nblk + slot / bs) * Hkv + h) * bs + slot % bs) * chunks + c;
+    const int64_t src = ((int64_t)t * Hkv + h) * chunks + c;
+    k_cache[dst] = k_new[src];
+    v_cache[dst] = v_new[src];
   }
-  const int sms = device_sm_count();
-  const int64_t grid = P.items < sms ? P.items : sms;
-  dcp_decode_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(tk, tv, P);
+}
+
+cudaError_t launch_paged_kv_write(const void* k_new, const void* v_new, const int64_t* slots,
+                                  void* k_cache, void* v_cache, int T, int Hkv, int D, int W,
+                                  int64_t nblk, int bs, int elem_bytes, cudaStream_t stream) {
+  const int chunks = D * elem_bytes / 16;
+  const int64_t total = (int64_t)W * T * Hkv * chunks;
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = (int64_t)device_sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  paged_kv_write_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      (const uint4*)k_new, (const uint4*)v_new, slots, (uint4*)k_cache, (uint4*)v_cache, T, Hkv,
+      chunks, W, nblk, bs);
   return cudaGetLastError();
 }
 

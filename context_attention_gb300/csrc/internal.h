@@ -73,10 +73,19 @@ struct DecodeArgs {
   float* o_parts;         // [W*splits, N*Hq, D]
   float* lse_parts;       // [W*splits, N*Hq]
   unsigned* err;
+  // paged cache (k, v are [W, nblk, Hkv, bs, D]; Lloc = max_blocks * bs)
+  int paged;
+  const int32_t* block_tables;  // [W, N, max_blocks]
+  int64_t nblk, max_blocks;
+  int bs;
 };
 cudaError_t launch_dcp_decode_partials(const DecodeArgs& a, cudaStream_t stream);
 // Decode split geometry shared by the workspace query and the launch.
 void dcp_decode_split(int64_t Lloc, int64_t* chunk, int* splits);
+
+cudaError_t launch_paged_kv_write(const void* k_new, const void* v_new, const int64_t* slots,
+                                  void* k_cache, void* v_cache, int T, int Hkv, int D, int W,
+                                  int64_t nblk, int bs, int elem_bytes, cudaStream_t stream);
 
 cudaError_t launch_permute_rows(const void* src, void* dst, int64_t BH, int64_t S,
                                 int64_t row_bytes, int cp, int layout, int to_shards,

@@ -230,6 +230,45 @@ ca_status ca_dcp_decode_noalloc(const void *q, const void *k_shards,
                                 void *stream);
 
 /* ------------------------------------------------------------------------
+ * DCP decode over paged KV caches ([DCP] "Slot Mapping and KV Cache",
+ * "Segmented Attention CP" step 1: KV read from the cache through the block
+ * table).  Same computation as ca_dcp_decode; rank r's local slot s of
+ * sequence n lives in block block_tables[r][n][s / block_size] of rank r's
+ * cache at offset s % block_size.
+ *
+ * k_cache, v_cache  device [dcp, nblk, Hkv, block_size, D] bf16 (one cache
+ *             per rank; blocks hold block_size consecutive slots per head).
+ * block_tables device int32 [dcp, N, max_blocks]; only the entries covering
+ *             a sequence's valid slots on a rank are read.
+ * seq_lens    device int32 [N] (required; at most dcp*max_blocks*block_size).
+ * workspace   ca_dcp_decode_workspace_size(N, Hq, Hkv,
+ *             max_blocks*block_size, D, dcp, interleave) bytes.
+ * Errors: CA_ERR_UNSUPPORTED unless bf16, D = 128, Hq/Hkv <= 8 and
+ * block_size in {8, 16, 32, 64, 128}.
+ * ---------------------------------------------------------------------- */
+ca_status ca_dcp_decode_paged(const void *q, const void *k_cache,
+                              const void *v_cache, const int32_t *block_tables,
+                              ca_dtype dtype, int N, int Hq, int Hkv,
+                              int64_t nblk, int block_size, int64_t max_blocks,
+                              int D, int dcp, int interleave,
+                              const int32_t *seq_lens, float softmax_scale,
+                              void *o, float *lse, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+/* Write new tokens' K/V into the paged caches by slot mapping ([DCP] "Active
+ * Token Handling and dcp_active_mask", "Slot Mapping and KV Cache"): token t
+ * goes to rank r's slot slots[r*T + t] (block slot / block_size, offset
+ * slot % block_size); -1 means rank r does not own the token and nothing is
+ * written.  Slots can come from ca_dcp_slot_mapping.  Bit-exact copies.
+ * k_new, v_new device [T, Hkv, D]; slots device int64 [dcp, T];
+ * k_cache, v_cache device [dcp, nblk, Hkv, block_size, D]; D*elem % 16 == 0.
+ * Slots whose block is >= nblk are skipped. */
+ca_status ca_paged_kv_write(const void *k_new, const void *v_new,
+                            const int64_t *slots, void *k_cache, void *v_cache,
+                            ca_dtype dtype, int T, int Hkv, int D, int dcp,
+                            int64_t nblk, int block_size, void *stream);
+
+/* ------------------------------------------------------------------------
  * DCP prefill of one chunk ([DCP] "Segmented Attention CP", "DCP Prefill"
  * compute pattern): the chunk's Sc gathered queries (global positions
  * P .. P+Sc-1, P = prior_tokens) attend, on every rank R, to R's local KV --
