@@ -58,8 +58,13 @@ constexpr uint32_t kSmemQ = 0;
 constexpr uint32_t kSmemKV = 2 * kTileBytes;
 constexpr uint32_t kSmemBar = kSmemKV + kNSlot * kTileBytes;
 // barrier indices
-constexpr int kBarKvFull = 0;
-constexpr int kBarKvEmpty = kBarKvFull + kNSlot;
+// Loads land on "group" barriers, one per tile: a unit's Q tiles and K_0 on
+// q_full; V_j together with K_(j+1) on tile_full[(t) % kNGroup], t the
+// CTA's running tile index.  The issuing thread then waits once per tile for
+// both operands of PV(j) and S(j+1).
+constexpr int kNGroup = 4;
+constexpr int kBarKvFull = 0;  // kNGroup tile barriers
+constexpr int kBarKvEmpty = kBarKvFull + kNGroup;
 constexpr int kBarQFull = kBarKvEmpty + kNSlot;
 constexpr int kBarQEmpty = kBarQFull + 1;
 constexpr int kBarSFull = kBarQEmpty + 1;   // 2
@@ -460,10 +465,8 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int s = 0; s < kNSlot; ++s) {
-      mbar_init(bar(kBarKvFull + s), 1);
-      mbar_init(bar(kBarKvEmpty + s), 1);  // arrived by softmax warpgroup 1
-    }
+    for (int s = 0; s < kNGroup; ++s) mbar_init(bar(kBarKvFull + s), 1);
+    for (int s = 0; s < kNSlot; ++s) mbar_init(bar(kBarKvEmpty + s), 1);  // arrived by softmax warpgroup 1
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
     for (int i = 0; i < 2; ++i) {
@@ -489,54 +492,80 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
+    int64_t kvh_of = 0;  // key/value head of the current unit (3-D maps)
     if (lane == 0) {
       uint32_t uc = 0;
-      uint64_t pos = 0;
+      uint64_t pos = 0, gt = 0;
+      uint64_t armed = 0;    // tile barriers armed so far (running tile index)
+      uint32_t q_armed = 0;  // times q_full was armed
       bool ok = true;
+      // wait until ring position `pos + d` is free
+      auto slot_free = [&](uint64_t d) -> bool {
+        const uint64_t p = pos + d;
+        return mbar_wait(bar(kBarKvEmpty + (int)(p % kNSlot)), (uint32_t)(((p / kNSlot) & 1) ^ 1),
+                         abort_flag, err);
+      };
+      // K (kv = 0) or V (kv = 1) tile kt of step `st` into ring position
+      // `pos`, completing on barrier `fb`
+      auto load_kv = [&](const Step& st, int kt, int kv, uint32_t fb) {
+        const int slot = (int)(pos % kNSlot);
+        const CUtensorMap* m = &maps.kv[2 * st.src + kv];
+        const int krow = (int)(st.row0 + (int64_t)kt * kBN);
+        for (int hx = 0; hx < 2; ++hx) {
+          const uint32_t dst = sbase + kSmemKV + slot * kTileBytes + hx * kBoxBytes;
+          if (P.seg)
+            tma_load_3d(dst, m, fb, hx * 64, krow, (int)kvh_of);
+          else
+            tma_load_2d(dst, m, fb, hx * 64, krow);
+        }
+        ++pos;
+      };
+      // Every barrier is armed only once all slots its copies go to are
+      // free, so an armed barrier always completes.
       for (int64_t k = 0, u = unit_at(P, 0); u < P.units && ok; ++k, u = unit_at(P, k)) {
         const Unit U = unit_of(P, u);
         const int n = unit_tiles(P, U);
         if (n == 0) continue;
-        ok = mbar_wait(bar(kBarQEmpty), (uc & 1) ^ 1, abort_flag, err);
+        kvh_of = U.bhk;
+        ok = mbar_wait(bar(kBarQEmpty), (uc & 1) ^ 1, abort_flag, err) && slot_free(0);
         if (!ok) break;
-        mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes);
+        TileIter it;
+        it.begin(P, U);
+        // Q tiles and K_0 on q_full
+        mbar_arrive_expect_tx(bar(kBarQFull), 3 * kTileBytes);
+        ++q_armed;
         const int qrow = (int)(U.bh * P.a.Sq + (int64_t)U.r_store * P.a.Ls + U.qrow0);
         for (int i = 0; i < 2; ++i)
           for (int hx = 0; hx < 2; ++hx)
             tma_load_2d(sbase + kSmemQ + i * kTileBytes + hx * kBoxBytes, &maps.q, bar(kBarQFull),
                         hx * 64, qrow + i * kBM);
-        TileIter it;
-        it.begin(P, U);
-        for (int j = 0; j < n && ok; ++j) {
-          const int krow = (int)(it.st.row0 + (int64_t)it.kt * kBN);
-          const int kvh = (int)(U.bhk);
-          for (int kv = 0; kv < 2 && ok; ++kv) {
-            const int slot = (int)(pos % kNSlot);
-            const uint32_t ph = (uint32_t)((pos / kNSlot) & 1);
-            ok = mbar_wait(bar(kBarKvEmpty + slot), ph ^ 1, abort_flag, err);
-            if (!ok) break;
-            mbar_arrive_expect_tx(bar(kBarKvFull + slot), kTileBytes);
-            const CUtensorMap* m = &maps.kv[2 * it.st.src + kv];
-            for (int hx = 0; hx < 2; ++hx) {
-              if (P.seg)
-                tma_load_3d(sbase + kSmemKV + slot * kTileBytes + hx * kBoxBytes, m,
-                            bar(kBarKvFull + slot), hx * 64, krow, kvh);
-              else
-                tma_load_2d(sbase + kSmemKV + slot * kTileBytes + hx * kBoxBytes, m,
-                            bar(kBarKvFull + slot), hx * 64, krow);
-            }
-            ++pos;
-          }
+        load_kv(it.st, it.kt, 0, bar(kBarQFull));
+        // V_j and K_(j+1) on the tile barrier of tile j.  The barrier's
+        // previous phase (tile t - kNGroup) was waited for by the issuing
+        // thread before it consumed the older tiles whose slots are free now.
+        for (int j = 0; j < n; ++j) {
+          const uint64_t t = gt + j;
+          const uint32_t fb = bar(kBarKvFull + (int)(t % kNGroup));
+          const Step stj = it.st;
+          const int ktj = it.kt;
           it.next(P, U);
+          const bool more = j + 1 < n;
+          ok = slot_free(0) && (!more || slot_free(1));
+          if (!ok) break;
+          mbar_arrive_expect_tx(fb, (more ? 2u : 1u) * kTileBytes);
+          ++armed;
+          load_kv(stj, ktj, 1, fb);
+          if (more) load_kv(it.st, it.kt, 0, fb);
         }
+        gt += n;
         ++uc;
       }
       if (!ok) {
         // error path: let the copies already in flight land before exit
-        for (uint64_t p = pos > kNSlot ? pos - kNSlot : 0; p < pos; ++p) {
-          volatile int never = 0;
-          mbar_wait(bar(kBarKvFull + (int)(p % kNSlot)), (uint32_t)((p / kNSlot) & 1), &never, err);
-        }
+        volatile int never = 0;
+        for (uint64_t t = armed > kNGroup ? armed - kNGroup : 0; t < armed; ++t)
+          mbar_wait(bar(kBarKvFull + (int)(t % kNGroup)), (uint32_t)((t / kNGroup) & 1), &never, err);
+        if (q_armed) mbar_wait(bar(kBarQFull), (q_armed - 1) & 1, &never, err);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -558,13 +587,11 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         const Unit U = unit_of(P, u);
         const int n = unit_tiles(P, U);
         if (n == 0) continue;
+        // Q tiles and K_0
         ok = mbar_wait(bar(kBarQFull), uc & 1, abort_flag, err);
         if (!ok) break;
         tc_fence_after();
         int kslot = (int)(pos % kNSlot);
-        ok = mbar_wait(bar(kBarKvFull + kslot), (uint32_t)((pos / kNSlot) & 1), abort_flag, err);
-        if (!ok) break;
-        tc_fence_after();
         issue_s(tS0, qdesc0, kd(kslot));
         tc_commit(bar(kBarSFull + 0));
         issue_s(tS1, qdesc1, kd(kslot));
@@ -572,7 +599,9 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         ++pos;
         for (int j = 0; j < n && ok; ++j) {
           const int vslot = (int)(pos % kNSlot);
-          ok = mbar_wait(bar(kBarKvFull + vslot), (uint32_t)((pos / kNSlot) & 1), abort_flag, err);
+          // V_j and K_(j+1)
+          const uint64_t t = gt + j;
+          ok = mbar_wait(bar(kBarKvFull + (int)(t % kNGroup)), (uint32_t)((t / kNGroup) & 1), abort_flag, err);
           if (!ok) break;
           const uint32_t pph = (uint32_t)((gt + j) & 1);
           ok = mbar_wait(bar(kBarPFull + 0), pph, abort_flag, err);
@@ -583,9 +612,6 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
           const bool more = j + 1 < n;
           if (more) {
             kslot = (int)(pos % kNSlot);
-            ok = mbar_wait(bar(kBarKvFull + kslot), (uint32_t)((pos / kNSlot) & 1), abort_flag, err);
-            if (!ok) break;
-            tc_fence_after();
             issue_s(tS0, qdesc0, kd(kslot));
             tc_commit(bar(kBarSFull + 0));
           } else {
