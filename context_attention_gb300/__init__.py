@@ -72,6 +72,8 @@ def _load():
             "ca_ring_attn_fwd_workspace_size": ([I, I, I, I64, I, I, I], SZ),
             "ca_ring_attn_fwd": ([P, P, P, P, P, I, I, I, I, I64, I, I, I, I, I, F, P, SZ, P], I),
             "ca_ring_attn_fwd_bounded": ([P, P, P, P, P, P, I, I, I, I, I64, I, I, I, I, F, P], I),
+            "ca_ring_attn_fwd_kmax": ([P, P, P, P, P, P, I, I, I, I, I64, I, I, I, I, F, P], I),
+            "ca_key_max2": ([P, I, I, I, I64, I, P, P], I),
             "ca_attn_partial_step": ([P, P, P, I, I, I, I, I64, I, I, I, I, I, I, I, F, P, P, P, P], I),
             "ca_lse_merge": ([P, P, I, I64, I, P, P, I, P, P], I),
             "ca_const_max_bound": ([P, P, I, I, I, I, I64, I, F, P, P, P], I),
@@ -177,6 +179,28 @@ def ring_attn_fwd_bounded(q, k, v, c, cp_size, causal=False, layout="contiguous"
     return out, (lse if return_lse else None)
 
 
+def ring_attn_fwd_kmax(q, k, v, kmax2, cp_size, causal=False, layout="contiguous", softmax_scale=None,
+                       out=None, lse=None, return_lse=True):
+    """Const-max ring attention with a caller-provided key maximum kmax2
+    [B,Hkv] fp32 (max |k_j|^2 per head, e.g. from key_max2, or its max over
+    processes); each row's bound is formed in the kernel."""
+    lib = _load()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, n, 4)
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty(B, Hq, S, device=q.device, dtype=torch.float32)
+    st = lib.ca_ring_attn_fwd_kmax(_ptr(q), _ptr(k), _ptr(v), _ptr(kmax2.contiguous()), _ptr(out),
+                                   _ptr(lse if return_lse else None), DTYPE[q.dtype], B, Hq, Hkv, S, D,
+                                   cp_size, int(bool(causal)), LAYOUT[layout], float(softmax_scale or 0.0),
+                                   _stream(q))
+    _check("ca_ring_attn_fwd_kmax", st)
+    return out, (lse if return_lse else None)
+
+
 def attn_partial_step(q_shard, k_shard, v_shard, q_rank, kv_rank, cp_size, mode="online_max",
                       causal=False, layout="contiguous", softmax_scale=None, c=None):
     """One ring step: queries of shard q_rank against the K/V of shard kv_rank.
@@ -215,6 +239,18 @@ def lse_merge(o_parts, lse_parts, c=None, out_dtype=torch.float32):
                           _ptr(lse), _stream(o_parts))
     _check("ca_lse_merge", st)
     return o, lse
+
+
+def key_max2(k, out=None):
+    """kmax2 [B,Hkv] fp32: per head, the max over keys of |k_j|^2."""
+    lib = _load()
+    _need(k, "k", 4)
+    B, Hkv, S, D = k.shape
+    if out is None:
+        out = torch.empty(B, Hkv, device=k.device, dtype=torch.float32)
+    st = lib.ca_key_max2(_ptr(k), DTYPE[k.dtype], B, Hkv, S, D, _ptr(out), _stream(k))
+    _check("ca_key_max2", st)
+    return out
 
 
 def const_max_bound(q, k, softmax_scale=None):

@@ -119,10 +119,11 @@ size_t ca_ring_attn_fwd_workspace_size(int B, int Hq, int Hkv, int64_t S, int D,
   (void)D;
   (void)cp_size;
   if (mode != CA_MODE_CONST_MAX || B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0) return 0;
-  return align256(sizeof(float) * (size_t)B * Hq * S) + align256(sizeof(float) * (size_t)B * Hkv);
+  return align256(sizeof(float) * (size_t)B * Hkv);  // kmax2
 }
 
-static ca_status ring_common(const void* q, const void* k, const void* v, const float* c, void* o,
+static ca_status ring_common(const void* q, const void* k, const void* v, const float* c,
+                             const float* kmax2, void* o,
                              float* lse, ca_dtype dtype, int B, int Hq, int Hkv, int64_t S, int D,
                              int cp_size, ca_mode mode, int causal, ca_layout layout,
                              float softmax_scale, void* workspace, size_t workspace_bytes,
@@ -133,9 +134,10 @@ static ca_status ring_common(const void* q, const void* k, const void* v, const 
   if (st != CA_OK) return st;
   if (S % cp_size != 0) return CA_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
-      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) || (c && (reinterpret_cast<uintptr_t>(c) & 3u)))
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) || (c && (reinterpret_cast<uintptr_t>(c) & 3u)) ||
+      (kmax2 && (reinterpret_cast<uintptr_t>(kmax2) & 3u)))
     return CA_ERR_ALIGNMENT;
-  const bool own_bound = mode == CA_MODE_CONST_MAX && c == nullptr;
+  const bool own_bound = mode == CA_MODE_CONST_MAX && c == nullptr && kmax2 == nullptr;
   const size_t need = own_bound ? ca_ring_attn_fwd_workspace_size(B, Hq, Hkv, S, D, cp_size, mode) : 0;
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return CA_ERR_WORKSPACE;
@@ -165,19 +167,19 @@ static ca_status ring_common(const void* q, const void* k, const void* v, const 
   a.mode = (int)mode;
   a.scale = scale;
   a.c = c;
+  a.kmax2 = kmax2;
   a.o = o;
   a.out_f32 = dtype == CA_DTYPE_F32;
   a.unnormalized = 0;
   a.lse = lse;
   a.err = err;
   if (own_bound) {
-    float* cw = static_cast<float*>(workspace);
-    float* kmax2 = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                            align256(sizeof(float) * (size_t)B * Hq * S));
-    cudaError_t e = launch_const_max_bound(q, k, dtype == CA_DTYPE_BF16, B, Hq, Hkv, S, D, scale,
-                                           cw, kmax2, s);
+    // the key pass only: both kernels form each row's bound from the q rows
+    // they load anyway
+    float* kw = static_cast<float*>(workspace);
+    cudaError_t e = launch_key_max2(k, dtype == CA_DTYPE_BF16, B, Hkv, S, D, kw, s);
     if (e != cudaSuccess) return launched(e);
-    a.c = cw;
+    a.kmax2 = kw;
   }
   if (trace_enabled())
     fprintf(stderr, "[ctxattn] ring_attn_fwd dtype=%d B=%d Hq=%d Hkv=%d S=%lld D=%d cp=%d mode=%d causal=%d layout=%d\n",
@@ -189,8 +191,8 @@ ca_status ca_ring_attn_fwd(const void* q, const void* k, const void* v, void* o,
                            ca_dtype dtype, int B, int Hq, int Hkv, int64_t S, int D, int cp_size,
                            ca_mode mode, int causal, ca_layout layout, float softmax_scale,
                            void* workspace, size_t workspace_bytes, void* stream) {
-  return ring_common(q, k, v, nullptr, o, lse, dtype, B, Hq, Hkv, S, D, cp_size, mode, causal,
-                     layout, softmax_scale, workspace, workspace_bytes, stream);
+  return ring_common(q, k, v, nullptr, nullptr, o, lse, dtype, B, Hq, Hkv, S, D, cp_size, mode,
+                     causal, layout, softmax_scale, workspace, workspace_bytes, stream);
 }
 
 ca_status ca_ring_attn_fwd_bounded(const void* q, const void* k, const void* v, const float* c,
@@ -198,8 +200,17 @@ ca_status ca_ring_attn_fwd_bounded(const void* q, const void* k, const void* v, 
                                    int64_t S, int D, int cp_size, int causal, ca_layout layout,
                                    float softmax_scale, void* stream) {
   if (!c) return CA_ERR_INVALID_ARG;
-  return ring_common(q, k, v, c, o, lse, dtype, B, Hq, Hkv, S, D, cp_size, CA_MODE_CONST_MAX,
-                     causal, layout, softmax_scale, nullptr, 0, stream);
+  return ring_common(q, k, v, c, nullptr, o, lse, dtype, B, Hq, Hkv, S, D, cp_size,
+                     CA_MODE_CONST_MAX, causal, layout, softmax_scale, nullptr, 0, stream);
+}
+
+ca_status ca_ring_attn_fwd_kmax(const void* q, const void* k, const void* v, const float* kmax2,
+                                void* o, float* lse, ca_dtype dtype, int B, int Hq, int Hkv,
+                                int64_t S, int D, int cp_size, int causal, ca_layout layout,
+                                float softmax_scale, void* stream) {
+  if (!kmax2) return CA_ERR_INVALID_ARG;
+  return ring_common(q, k, v, nullptr, kmax2, o, lse, dtype, B, Hq, Hkv, S, D, cp_size,
+                     CA_MODE_CONST_MAX, causal, layout, softmax_scale, nullptr, 0, stream);
 }
 
 ca_status ca_attn_partial_step(const void* q_shard, const void* k_shard, const void* v_shard,
@@ -275,6 +286,15 @@ ca_status ca_const_max_bound(const void* q, const void* k, ca_dtype dtype, int B
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
   return launched(launch_const_max_bound(q, k, dtype == CA_DTYPE_BF16, B, Hq, Hkv, S, D, scale, c,
                                          kmax2, static_cast<cudaStream_t>(stream)));
+}
+
+ca_status ca_key_max2(const void* k, ca_dtype dtype, int B, int Hkv, int64_t S, int D, float* kmax2,
+                      void* stream) {
+  if (!k || !kmax2) return CA_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || B <= 0 || Hkv <= 0 || S <= 0 || D <= 0) return CA_ERR_INVALID_ARG;
+  if (!aligned16(k) || (reinterpret_cast<uintptr_t>(kmax2) & 3u)) return CA_ERR_ALIGNMENT;
+  return launched(launch_key_max2(k, dtype == CA_DTYPE_BF16, B, Hkv, S, D, kmax2,
+                                  static_cast<cudaStream_t>(stream)));
 }
 
 // ------------------------------------------------------------------ decode

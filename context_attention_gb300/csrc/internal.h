@@ -23,6 +23,9 @@ struct RingArgs {
   int causal, layout, mode;
   float scale;        // softmax scale
   const float* c;     // const-max bound [B, Hq, Sq] (natural units) or null
+  // const max with c == null: per (batch, kv head) max |k|^2 [B, Hkv]; the
+  // kernel forms each row's bound from the q tile it already holds
+  const float* kmax2 = nullptr;
   void* o;            // output
   int out_f32;        // 1: fp32 output rows, 0: input dtype (bf16)
   int unnormalized;   // const-max step: write acc_o instead of acc_o / acc_l
@@ -52,6 +55,9 @@ constexpr int kDcpPrefillMaxRanks = 8;
 cudaError_t launch_dcp_prefill_tc(const DcpPrefillArgs& d, cudaStream_t stream);
 cudaError_t launch_ring_simt_f32(const RingArgs& a, cudaStream_t stream);
 
+// kmax2[b, hk] = max over the S keys of |k|^2 (zeroes kmax2 first).
+cudaError_t launch_key_max2(const void* k, int is_bf16, int B, int Hkv, int64_t S, int D,
+                            float* kmax2, cudaStream_t stream);
 cudaError_t launch_const_max_bound(const void* q, const void* k, int is_bf16, int B,
                                    int Hq, int Hkv, int64_t S, int D, float scale,
                                    float* c, float* kmax2, cudaStream_t stream);

@@ -58,9 +58,21 @@ ring_simt_kernel(RingArgs a, int qblocks) {
     m[rr] = -INFINITY;
     l[rr] = 0.f;
     cst[rr] = 0.f;
-    if (a.mode == 1 && arow[rr] < a.Ls)
+    if (a.mode == 1 && !a.kmax2 && arow[rr] < a.Ls)
       cst[rr] = a.c[bh * a.Sq + (int64_t)r_store * a.Ls + arow[rr]];
     for (int i = 0; i < kDPer; ++i) o[rr][i] = 0.f;
+  }
+  if (a.mode == 1 && a.kmax2) {
+    // each row's bound from its staged q row: c = sqrt(scale^2 * kmax2 * |q|^2)
+    __syncthreads();
+    const float km = a.kmax2[bhk];
+    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+      const float* qr = sq + (warp * kRowsPerWarp + rr) * D;
+      float ss = 0.f;
+      for (int d = lane; d < D; d += 32) ss = fmaf(qr[d], qr[d], ss);
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      cst[rr] = sqrtf(a.scale * a.scale * km * ss);
+    }
   }
   const int64_t a_last = min(a0 + kRows - 1, a.Ls - 1);
   const int nsteps = a.kv_rank_fixed >= 0 ? 1 : a.cp;

@@ -468,7 +468,10 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
     for (int s = 0; s < kNGroup; ++s) mbar_init(bar(kBarKvFull + s), 1);
     for (int s = 0; s < kNSlot; ++s) mbar_init(bar(kBarKvEmpty + s), 1);  // arrived by softmax warpgroup 1
     mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQEmpty), 1);
+    // the Q tiles are released by softmax warpgroup 1 after the last S MMA
+    // and, when the softmax warps read them for the row bounds, by each of
+    // those eight warps too
+    mbar_init(bar(kBarQEmpty), (P.a.mode == 1 && P.a.kmax2) ? 1 + 8 : 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarPFull + i), kBM);
@@ -673,7 +676,36 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         continue;
       }
       float c_nat = 0.f;
-      if (const_max && valid) c_nat = P.a.c[orow];
+      if (const_max && P.a.kmax2) {
+        // the row's bound from its q row in the Q tile: |q|^2 summed in fp32
+        // (the order of the 16-byte chunks is the swizzled one; a sum does
+        // not care), c = sqrt(scale^2 * kmax2 * |q|^2)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQFull), uc & 1, abort_flag, err));
+        if (!ok) break;
+        float ss = 0.f;
+#pragma unroll
+        for (int hx = 0; hx < 2; ++hx) {
+          const uint4* row =
+              reinterpret_cast<const uint4*>(smem + kSmemQ + i * kTileBytes + hx * kBoxBytes + tid * 128);
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 w = row[ch];
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = __uint_as_float(ws[e] << 16), hi = __uint_as_float(ws[e] & 0xFFFF0000u);
+              ss = fmaf(lo, lo, ss);
+              ss = fmaf(hi, hi, ss);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarQEmpty));
+        const float km = P.a.kmax2[U.bhk];
+        c_nat = sqrtf(P.a.scale * P.a.scale * km * ss);
+      } else if (const_max && valid) {
+        c_nat = P.a.c[orow];
+      }
       const float c_log2 = c_nat * kLog2e;
       float m = -INFINITY;  // reference max, log2 units (online mode)
       float l = 0.f;

@@ -95,7 +95,11 @@ int ca_version(void);
  * lse         device, [B,Hq,S] fp32, or NULL.
  * softmax_scale  <= 0 selects 1/sqrt(D).
  * workspace   device, at least ca_ring_attn_fwd_workspace_size() bytes
- *             (may be NULL when that size is 0).
+ *             (may be NULL when that size is 0).  Const max uses it for
+ *             kmax2 [B,Hkv]: one streaming pass over k (ca_key_max2), after
+ *             which the attention kernel forms each row's bound from the q
+ *             row it has loaded anyway ([CM] "Best practices": side
+ *             quantities inside a pass already paid for).
  * Errors: CA_ERR_SHAPE if S % cp_size != 0 ([CP] "Sequence Length
  * Constraints": S=3645 with cp_size=8 is rejected) or Hq % Hkv != 0;
  * CA_ERR_UNSUPPORTED for bf16 with D != 128.
@@ -120,6 +124,20 @@ ca_status ca_ring_attn_fwd_bounded(const void *q, const void *k, const void *v,
                                    int64_t S, int D, int cp_size, int causal,
                                    ca_layout layout, float softmax_scale,
                                    void *stream);
+
+/* Ring attention in const-max mode with a caller-provided key maximum
+ * kmax2 [B,Hkv] fp32 (device): max over all keys of the head of |k_j|^2, as
+ * ca_key_max2 gives it for local keys; a caller whose keys span several
+ * processes takes the elementwise max of their kmax2 first ([CM] "Global
+ * key max": one all-reduce(max) of one value per head).  The kernel forms
+ * c_i = sqrt(scale^2 * kmax2 * |q_i|^2) from each q row it loads.  Same
+ * output as ca_ring_attn_fwd(mode = CA_MODE_CONST_MAX); no workspace. */
+ca_status ca_ring_attn_fwd_kmax(const void *q, const void *k, const void *v,
+                                const float *kmax2, void *o, float *lse,
+                                ca_dtype dtype, int B, int Hq, int Hkv,
+                                int64_t S, int D, int cp_size, int causal,
+                                ca_layout layout, float softmax_scale,
+                                void *stream);
 
 /* ------------------------------------------------------------------------
  * One ring step ([CM] "Overview", step t: acc_r += attn(Q_r, K_{r-t},
@@ -163,6 +181,19 @@ ca_status ca_attn_partial_step(const void *q_shard, const void *k_shard,
 ca_status ca_lse_merge(const float *o_parts, const float *lse_parts, int n,
                        int64_t R, int D, const float *c, void *o,
                        ca_dtype out_dtype, float *lse, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Key maximum of the const-max bound ([CM] "Global key max", "Transpose
+ * prologue with fused norms": per head, the running max of |k_j|^2):
+ * kmax2[b,hk] = max over the S rows of k[b,hk] of |k_j|^2, squares summed in
+ * fp32.  kmax2 is zeroed first, then reduced into (an fp32 max of
+ * non-negative values, exact whatever the order).
+ *
+ * k           device [B,Hkv,S,D], dtype, 16-byte aligned.
+ * kmax2       device [B,Hkv] fp32 (output), 4-byte aligned.
+ * ---------------------------------------------------------------------- */
+ca_status ca_key_max2(const void *k, ca_dtype dtype, int B, int Hkv, int64_t S,
+                      int D, float *kmax2, void *stream);
 
 /* ------------------------------------------------------------------------
  * Const-max bound ([CM] "Picking a max ...", "Global key max", "Assembling

@@ -66,9 +66,33 @@ def test_ring_validation_codes(ca):
     assert S[ring(lib, q=FAKE + 2)] == "CA_ERR_ALIGNMENT"
     assert S[ring(lib, mode=1)] == "CA_ERR_WORKSPACE"            # const max needs the bound buffer
     need = lib.ca_ring_attn_fwd_workspace_size(1, 4, 2, 1024, 128, 4, 1)
-    assert need >= 4 * 4 * 1024
+    assert need >= 4 * 2                                         # kmax2 [B, Hkv]
     assert S[ring(lib, mode=1, ws=FAKE, ws_bytes=need - 1)] == "CA_ERR_WORKSPACE"
     assert lib.ca_ring_attn_fwd_workspace_size(1, 4, 2, 1024, 128, 4, 0) == 0
+
+
+def test_key_max_and_kmax_ring_validation(ca):
+    lib = ca._load()
+    S = ca.STATUS
+    assert S[lib.ca_key_max2(None, 1, 1, 2, 1024, 128, FAKE, None)] == "CA_ERR_INVALID_ARG"
+    assert S[lib.ca_key_max2(FAKE, 1, 1, 2, 0, 128, FAKE, None)] == "CA_ERR_INVALID_ARG"
+    assert S[lib.ca_key_max2(FAKE, 3, 1, 2, 1024, 128, FAKE, None)] == "CA_ERR_INVALID_ARG"
+    assert S[lib.ca_key_max2(FAKE + 4, 1, 1, 2, 1024, 128, FAKE, None)] == "CA_ERR_ALIGNMENT"
+    assert S[lib.ca_key_max2(FAKE, 1, 1, 2, 1024, 128, FAKE + 2, None)] == "CA_ERR_ALIGNMENT"
+
+    def kring(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, km=FAKE, o=FAKE, lse=None, dtype=1, B=1, Hq=4, Hkv=2, S=1024, D=128,
+                 cp=4, causal=0, layout=0, scale=0.0)
+        a.update(kw)
+        return lib.ca_ring_attn_fwd_kmax(a["q"], a["k"], a["v"], a["km"], a["o"], a["lse"], a["dtype"], a["B"],
+                                         a["Hq"], a["Hkv"], a["S"], a["D"], a["cp"], a["causal"], a["layout"],
+                                         a["scale"], None)
+
+    assert S[kring(km=None)] == "CA_ERR_INVALID_ARG"
+    assert S[kring(S=1020, cp=8)] == "CA_ERR_SHAPE"
+    assert S[kring(Hq=6, Hkv=4)] == "CA_ERR_SHAPE"
+    assert S[kring(D=64)] == "CA_ERR_UNSUPPORTED"
+    assert S[kring(km=FAKE + 2)] == "CA_ERR_ALIGNMENT"
 
 
 def test_partial_step_validation_codes(ca):

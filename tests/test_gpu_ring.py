@@ -191,6 +191,75 @@ def test_const_max_bound_kernel(ca):
         np.testing.assert_allclose(np32(c), rc, rtol=2e-6)
 
 
+def test_key_max2_kernel(ca):
+    """kmax2 alone (vector paths with 32, 16 and 2 lanes a row, the scalar
+    path for rows not a multiple of 16 bytes, one-row heads)."""
+    from context_attention_gb300 import synth
+
+    for dtype, D, S in ((torch.bfloat16, 128, 700), (torch.float32, 128, 333), (torch.bfloat16, 48, 257),
+                        (torch.float32, 20, 700), (torch.bfloat16, 128, 1)):
+        _, k, _ = synth.normal_qkv(2, 2, 3, S, D, 12, dtype=dtype, device="cuda")
+        km = ca.key_max2(k)
+        _, rk = oracle.const_max_bound(np32(k), np32(k))
+        np.testing.assert_allclose(np32(km), rk, rtol=2e-6, err_msg=f"{dtype} D={D} S={S}")
+
+
+def test_key_max2_of_key_blocks_combines_by_max(ca):
+    """The per-process key maxima combine by an elementwise max (the
+    all-reduce of the const-max page's "Global key max"): bit-exact."""
+    from context_attention_gb300 import synth
+
+    _, k, _ = synth.normal_qkv(1, 4, 4, 4096, 128, 13, dtype=torch.bfloat16, device="cuda")
+    whole = ca.key_max2(k)
+    parts = [ca.key_max2(k[:, :, i * 1024:(i + 1) * 1024].contiguous()) for i in range(4)]
+    assert torch.equal(torch.stack(parts).amax(0), whole)
+
+
+def aligned_qk(B, Hq, Hkv, S, D, seed, alpha_max, beta, dtype):
+    """Keys and queries near one direction u per kv head, so the bound is
+    tight and large: s_ij ~ scale * alpha_i * beta, alpha_i log-uniform in
+    [1, alpha_max].  A bound off by tens of nats overflows or underflows."""
+    g = torch.Generator().manual_seed(seed)
+    G = Hq // Hkv
+    u = torch.randn(B, Hkv, 1, D, generator=g)
+    u = u / u.norm(dim=-1, keepdim=True)
+    k = beta * (u + 0.03 * torch.randn(B, Hkv, S, D, generator=g))
+    alpha = torch.exp(torch.rand(B, Hq, S, 1, generator=g) * np.log(alpha_max))
+    q = alpha * (u.repeat_interleave(G, dim=1) + 0.03 * torch.randn(B, Hq, S, D, generator=g))
+    v = torch.randn(B, Hkv, S, D, generator=g)
+    return (t.to(dtype).cuda() for t in (q, k, v))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("causal,layout", [(False, "contiguous"), (True, "contiguous"), (True, "striped")])
+def test_const_max_in_kernel_bound_large_scores(ca, dtype, causal, layout):
+    """Scores up to ~170 nats with a tight bound: only a correct per-row bound
+    formed in the kernel from kmax2 and the q row keeps exp(s - c) finite and
+    non-zero.  Fused entry (own key pass) and caller-provided kmax2 both match
+    the oracle; Ls = 300 is ragged."""
+    # bf16: D = 128, scores up to 0.088 * 48 * 40 = 170; fp32 (exact fp32
+    # scores must stay within 1e-4): D = 64, up to 0.125 * 48 * 16.7 = 100
+    D, beta = (128, 40.0) if dtype == torch.bfloat16 else (64, 16.7)
+    q, k, v = aligned_qk(2, 4, 2, 900, D, 14, 48.0, beta, dtype)
+    ro, rl = oracle_ring(q, k, v, 3, "const_max", causal, layout)
+    assert np.isfinite(rl).all() and rl.max() > 90
+    o, lse = ca.ring_attn_fwd(q, k, v, 3, mode="const_max", causal=causal, layout=layout)
+    assert_close(np32(o), ro, np32(lse), rl, dtype=dtype, what=f"fused {dtype} {layout}")
+    o2, lse2 = ca.ring_attn_fwd_kmax(q, k, v, ca.key_max2(k), 3, causal=causal, layout=layout)
+    assert_close(np32(o2), ro, np32(lse2), rl, dtype=dtype, what=f"kmax {dtype} {layout}")
+
+
+def test_const_max_in_kernel_bound_equals_given_bound(ca):
+    """The row bound formed in the kernel and the one ca_const_max_bound
+    writes agree to fp32 rounding, so the two entry points agree."""
+    q, k, v = aligned_qk(1, 8, 2, 2048, 128, 15, 30.0, 40.0, torch.bfloat16)
+    c, km = ca.const_max_bound(q, k)
+    o1, l1 = ca.ring_attn_fwd_bounded(q, k, v, c, 4)
+    o2, l2 = ca.ring_attn_fwd_kmax(q, k, v, km, 4)
+    np.testing.assert_allclose(np32(l2), np32(l1), rtol=0, atol=2e-5)
+    assert (np32(o2) - np32(o1)).__abs__().max() <= 1e-2
+
+
 # --------------------------------------------------------------- layouts (bit-exact)
 
 
