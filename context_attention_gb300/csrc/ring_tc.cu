@@ -259,29 +259,34 @@ struct TileIter {
 // further along inside a half (+2 in 16-byte descriptor units) and the second
 // half 16 KB further (+1024).  All eight issue from one asm block with the
 // descriptors advanced by 64-bit adds, keeping the issuing thread's own
-// instruction count (and so its share of contended issue slots) small.
+// instruction count (and so its share of contended issue slots) small.  The
+// whole warp executes the block with warp-uniform operands; only lane 0
+// issues.
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc) {
   asm volatile(
       "{\n\t"
-      ".reg .pred pf, pt;\n\t"
+      ".reg .pred pf, pt, pl;\n\t"
+      ".reg .b32 ln;\n\t"
+      "mov.u32 ln, %%laneid;\n\t"
+      "setp.eq.u32 pl, ln, 0;\n\t"
       ".reg .b64 a, b;\n\t"
       "setp.ne.b32 pf, %3, %3;\n\t"
       "setp.eq.b32 pt, %3, %3;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
       "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
       "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
       "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
       "add.s64 a, %1, 1024;\n\tadd.s64 b, %2, 1024;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
       "add.s64 a, %1, 1026;\n\tadd.s64 b, %2, 1026;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
       "add.s64 a, %1, 1028;\n\tadd.s64 b, %2, 1028;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
       "add.s64 a, %1, 1030;\n\tadd.s64 b, %2, 1030;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, pt;\n\t"
       "}" ::"r"(d_tmem),
       "l"(qdesc), "l"(kdesc), "n"(kIdescS)
       : "memory");
@@ -295,26 +300,29 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
                                          uint32_t acc) {
   asm volatile(
       "{\n\t"
-      ".reg .pred pa, pt;\n\t"
+      ".reg .pred pa, pt, pl;\n\t"
+      ".reg .b32 ln;\n\t"
+      "mov.u32 ln, %%laneid;\n\t"
+      "setp.eq.u32 pl, ln, 0;\n\t"
       ".reg .b64 b;\n\t"
       ".reg .b32 a;\n\t"
       "setp.ne.b32 pa, %3, 0;\n\t"
       "setp.eq.b32 pt, %3, %3;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, pa;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, pa;\n\t"
       "add.s32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
       "add.s32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
       "add.s32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
       "add.s32 a, %1, 32;\n\tadd.s64 b, %2, 512;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
       "add.s32 a, %1, 40;\n\tadd.s64 b, %2, 640;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
       "add.s32 a, %1, 48;\n\tadd.s64 b, %2, 768;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
       "add.s32 a, %1, 56;\n\tadd.s64 b, %2, 896;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %4, pt;\n\t"
       "}" ::"r"(d_tmem),
       "r"(p_tmem), "l"(vdesc), "r"(acc), "n"(kIdescPV)
       : "memory");
@@ -374,6 +382,41 @@ __device__ __forceinline__ float row_max_from_tmem(uint32_t tS, int vis_max) {
   tmem_ld_wait();
   reg_fence(rb);
   return chunk_max<kMask>(rb, 96, vis_max, mx);
+}
+
+// 4x4 transpose of 16-byte blocks inside each group of four lanes.  On
+// entry a[k] is block k of this lane's 64 bytes; on exit a[i] is block
+// (lane % 4) of the 64 bytes lane (lane & ~3) + i held.  Four lanes then
+// write four consecutive blocks of one row: whole 32-byte sectors.
+__device__ __forceinline__ uint4 shfl_xor_u4(uint4 v, int m) {
+  v.x = __shfl_xor_sync(0xffffffffu, v.x, m);
+  v.y = __shfl_xor_sync(0xffffffffu, v.y, m);
+  v.z = __shfl_xor_sync(0xffffffffu, v.z, m);
+  v.w = __shfl_xor_sync(0xffffffffu, v.w, m);
+  return v;
+}
+__device__ __forceinline__ void quad_transpose(uint4 (&a)[4], int lane) {
+  const bool b1 = (lane & 2) != 0, b0 = (lane & 1) != 0;
+  // exchange the off-diagonal 2x2 blocks with lane ^ 2
+  uint4 r0 = shfl_xor_u4(b1 ? a[0] : a[2], 2);
+  uint4 r1 = shfl_xor_u4(b1 ? a[1] : a[3], 2);
+  if (b1) {
+    a[0] = r0;
+    a[1] = r1;
+  } else {
+    a[2] = r0;
+    a[3] = r1;
+  }
+  // exchange inside each 2x2 block with lane ^ 1
+  r0 = shfl_xor_u4(b0 ? a[0] : a[1], 1);
+  r1 = shfl_xor_u4(b0 ? a[2] : a[3], 1);
+  if (b0) {
+    a[0] = r0;
+    a[2] = r1;
+  } else {
+    a[1] = r0;
+    a[3] = r1;
+  }
 }
 
 // Packed fp32 pair arithmetic (one instruction for two lanes of data), used
@@ -543,6 +586,13 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
             tma_load_2d(sbase + kSmemQ + i * kTileBytes + hx * kBoxBytes, &maps.q, bar(kBarQFull),
                         hx * 64, qrow + i * kBM);
         load_kv(it.st, it.kt, 0, bar(kBarQFull));
+        // the next unit's Q tiles come from HBM: start them towards L2 now
+        if (unit_at(P, k + 1) < P.units) {
+          const Unit N = unit_of(P, unit_at(P, k + 1));
+          const int nrow = (int)(N.bh * P.a.Sq + (int64_t)N.r_store * P.a.Ls + N.qrow0);
+          for (int i = 0; i < 2; ++i)
+            for (int hx = 0; hx < 2; ++hx) tma_prefetch_2d(&maps.q, hx * 64, nrow + i * kBM);
+        }
         // V_j and K_(j+1) on the tile barrier of tile j.  The barrier's
         // previous phase (tile t - kNGroup) was waited for by the issuing
         // thread before it consumed the older tiles whose slots are free now.
@@ -573,7 +623,9 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp walks the schedule, so every descriptor and TMEM
+    // address stays warp-uniform; lane 0 alone issues the MMAs and commits.
+    {
       uint32_t uc = 0;
       uint64_t pos = 0, gt = 0;
       bool ok = true;
@@ -591,23 +643,23 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         const int n = unit_tiles(P, U);
         if (n == 0) continue;
         // Q tiles and K_0
-        ok = mbar_wait(bar(kBarQFull), uc & 1, abort_flag, err);
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQFull), uc & 1, abort_flag, err));
         if (!ok) break;
         tc_fence_after();
         int kslot = (int)(pos % kNSlot);
         issue_s(tS0, qdesc0, kd(kslot));
-        tc_commit(bar(kBarSFull + 0));
+        tc_commit_lane0(bar(kBarSFull + 0));
         issue_s(tS1, qdesc1, kd(kslot));
-        tc_commit(bar(kBarSFull + 1));
+        tc_commit_lane0(bar(kBarSFull + 1));
         ++pos;
         for (int j = 0; j < n && ok; ++j) {
           const int vslot = (int)(pos % kNSlot);
           // V_j and K_(j+1)
           const uint64_t t = gt + j;
-          ok = mbar_wait(bar(kBarKvFull + (int)(t % kNGroup)), (uint32_t)((t / kNGroup) & 1), abort_flag, err);
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarKvFull + (int)(t % kNGroup)), (uint32_t)((t / kNGroup) & 1), abort_flag, err));
           if (!ok) break;
           const uint32_t pph = (uint32_t)((gt + j) & 1);
-          ok = mbar_wait(bar(kBarPFull + 0), pph, abort_flag, err);
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarPFull + 0), pph, abort_flag, err));
           if (!ok) break;
           tc_fence_after();
           issue_pv(tO0, tS0, vd(vslot), j > 0);
@@ -616,20 +668,20 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
           if (more) {
             kslot = (int)(pos % kNSlot);
             issue_s(tS0, qdesc0, kd(kslot));
-            tc_commit(bar(kBarSFull + 0));
+            tc_commit_lane0(bar(kBarSFull + 0));
           } else {
-            tc_commit(bar(kBarOFull + 0));
+            tc_commit_lane0(bar(kBarOFull + 0));
           }
-          ok = mbar_wait(bar(kBarPFull + 1), pph, abort_flag, err);
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarPFull + 1), pph, abort_flag, err));
           if (!ok) break;
           tc_fence_after();
           issue_pv(tO1, tS1, vd(vslot), j > 0);
           if (more) {
             issue_s(tS1, qdesc1, kd(kslot));
-            tc_commit(bar(kBarSFull + 1));
+            tc_commit_lane0(bar(kBarSFull + 1));
             ++pos;
           } else {
-            tc_commit(bar(kBarOFull + 1));
+            tc_commit_lane0(bar(kBarOFull + 1));
           }
         }
         gt += n;
@@ -787,21 +839,30 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         inv = 0.f;
         lse = -INFINITY;
       }
-#pragma unroll
-      for (int ch = 0; ch < kD / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tO + ch * 32, r);
-        tmem_ld_wait();
-        reg_fence(r);
-        if (valid) {
+      // the output row: the next 32 columns load from TMEM while the current
+      // ones are scaled, transposed inside lane quads and stored
+      {
+        const int qd = lane & 3;
+        uint32_t ra[32], rb[32];
+        auto emit = [&](const uint32_t(&r)[32], int ch) {
           if (P.a.out_f32) {
-            float4* dst = (float4*)((float*)P.a.o + orow * kD + ch * 32);
 #pragma unroll
-            for (int x = 0; x < 8; ++x)
-              dst[x] = make_float4(__uint_as_float(r[4 * x]) * inv, __uint_as_float(r[4 * x + 1]) * inv,
-                                   __uint_as_float(r[4 * x + 2]) * inv, __uint_as_float(r[4 * x + 3]) * inv);
+            for (int h = 0; h < 2; ++h) {
+              uint4 a4[4];
+#pragma unroll
+              for (int x = 0; x < 4; ++x)
+                a4[x] = make_uint4(__float_as_uint(__uint_as_float(r[16 * h + 4 * x]) * inv),
+                                   __float_as_uint(__uint_as_float(r[16 * h + 4 * x + 1]) * inv),
+                                   __float_as_uint(__uint_as_float(r[16 * h + 4 * x + 2]) * inv),
+                                   __float_as_uint(__uint_as_float(r[16 * h + 4 * x + 3]) * inv));
+              quad_transpose(a4, lane);
+#pragma unroll
+              for (int x = 0; x < 4; ++x)
+                if (a_row - qd + x < P.a.Ls)
+                  *(uint4*)((float*)P.a.o + (orow - qd + x) * kD + ch * 32 + h * 16 + qd * 4) = a4[x];
+            }
           } else {
-            uint4* dst = (uint4*)((__nv_bfloat16*)P.a.o + orow * kD + ch * 32);
+            uint4 a4[4];
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
               uint32_t w[4];
@@ -809,10 +870,31 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
               for (int y = 0; y < 4; ++y)
                 w[y] = pack_bf16x2(__uint_as_float(r[8 * x + 2 * y]) * inv,
                                    __uint_as_float(r[8 * x + 2 * y + 1]) * inv);
-              dst[x] = make_uint4(w[0], w[1], w[2], w[3]);
+              a4[x] = make_uint4(w[0], w[1], w[2], w[3]);
             }
+            quad_transpose(a4, lane);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              if (a_row - qd + x < P.a.Ls)
+                *(uint4*)((__nv_bfloat16*)P.a.o + (orow - qd + x) * kD + ch * 32 + qd * 8) = a4[x];
           }
-        }
+        };
+        tmem_ld32(tO, ra);
+        tmem_ld_wait();
+        reg_fence(ra);
+        tmem_ld32(tO + 32, rb);
+        emit(ra, 0);
+        tmem_ld_wait();
+        reg_fence(rb);
+        tmem_ld32(tO + 64, ra);
+        emit(rb, 1);
+        tmem_ld_wait();
+        reg_fence(ra);
+        tmem_ld32(tO + 96, rb);
+        emit(ra, 2);
+        tmem_ld_wait();
+        reg_fence(rb);
+        emit(rb, 3);
       }
       if (valid && P.a.lse) P.a.lse[orow] = lse;
       gt += n;
