@@ -465,6 +465,51 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&r)[32], int ch, int v
   tmem_st16(tS + ch * 16, pk);
 }
 
+// Online max, speculative single pass over one S row: p = 2^(s*sl2 - m)
+// against the row's current reference m, packed into registers (pk) and
+// summed into sum2, while the row maximum of the raw scores is tracked.
+// Nothing is written to TMEM, so if the maximum turns out to exceed the
+// lazy-rescale threshold the caller still has S to start over from.
+template <bool kMask>
+__device__ __forceinline__ float spec_row(uint32_t tS, int vis_max, uint64_t sl2_2, uint64_t nref_2,
+                                          uint32_t (&pk)[64], uint64_t& sum2) {
+  uint32_t ra[32], rb[32];
+  float mx = -INFINITY;
+  auto chunk = [&](const uint32_t(&r)[32], int ch) {
+    mx = chunk_max<kMask>(r, ch * 32, vis_max, mx);
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+      float s0 = __uint_as_float(r[2 * x]), s1 = __uint_as_float(r[2 * x + 1]);
+      if (kMask) {
+        if (ch * 32 + 2 * x > vis_max) s0 = -INFINITY;
+        if (ch * 32 + 2 * x + 1 > vis_max) s1 = -INFINITY;
+      }
+      float a0, a1;
+      f2_unpack(f2_fma(f2_pack(s0, s1), sl2_2, nref_2), a0, a1);
+      const float p0 = ex2(a0), p1 = ex2(a1);
+      sum2 = f2_add(sum2, f2_pack(p0, p1));
+      pk[16 * ch + x] = pack_bf16x2(p0, p1);
+    }
+  };
+  tmem_ld32(tS, ra);
+  tmem_ld_wait();
+  reg_fence(ra);
+  tmem_ld32(tS + 32, rb);
+  chunk(ra, 0);
+  tmem_ld_wait();
+  reg_fence(rb);
+  tmem_ld32(tS + 64, ra);
+  chunk(rb, 1);
+  tmem_ld_wait();
+  reg_fence(ra);
+  tmem_ld32(tS + 96, rb);
+  chunk(ra, 2);
+  tmem_ld_wait();
+  reg_fence(rb);
+  chunk(rb, 3);
+  return mx;
+}
+
 // Pass 2 over one S row: exp, row sum, P (bf16) back into TMEM, with the
 // next 32-column load in flight while the current chunk is processed.  P
 // block ch overwrites S columns [16ch, 16ch+16), which were already read.
@@ -781,9 +826,28 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         const int vis_max = (int)max((int64_t)-1, min(lim, (int64_t)(kBN - 1)));
         const bool need_mask = __any_sync(0xffffffffu, vis_max < kBN - 1);
         float mref;
+        bool p_done = false;  // P already in TMEM and its sum in l
         if (const_max) {
           mref = c_log2;
-        } else {
+        } else if (j > 0 && !__any_sync(0xffffffffu, m == -INFINITY)) {
+          // within a unit the row maximum rarely moves past the lazy-rescale
+          // threshold: try the single pass against the current reference
+          uint32_t pk[64];
+          const uint64_t sl2_2 = f2_pack(P.scale_log2, P.scale_log2), nref_2 = f2_pack(-m, -m);
+          uint64_t sum2 = f2_pack(0.f, 0.f);
+          const float mx = need_mask ? spec_row<true>(tS, vis_max, sl2_2, nref_2, pk, sum2)
+                                     : spec_row<false>(tS, vis_max, sl2_2, nref_2, pk, sum2);
+          if (__all_sync(0xffffffffu, !(mx * P.scale_log2 > m + kRescaleThreshold))) {
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) tmem_st16(tS + ch * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * ch]));
+            float lo, hi;
+            f2_unpack(sum2, lo, hi);
+            l += lo + hi;
+            p_done = true;
+          }
+          mref = m;
+        }
+        if (!const_max && !p_done) {
           // pass 1: row maximum straight from TMEM; the next 32-column load is
           // in flight while the current one is reduced
           float mx = need_mask ? row_max_from_tmem<true>(tS, vis_max) : row_max_from_tmem<false>(tS, vis_max);
@@ -814,9 +878,11 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         }
         // pass 2: p = 2^(s*scale*log2e - ref), row sum, bf16 P written over
         // the S columns already consumed (P column block ch < S block ch+1)
-        const float psum = need_mask ? exp_row_to_tmem<true>(tS, vis_max, P.scale_log2, mref)
-                                     : exp_row_to_tmem<false>(tS, vis_max, P.scale_log2, mref);
-        l += psum;
+        if (!p_done) {
+          const float psum = need_mask ? exp_row_to_tmem<true>(tS, vis_max, P.scale_log2, mref)
+                                       : exp_row_to_tmem<false>(tS, vis_max, P.scale_log2, mref);
+          l += psum;
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(kBarPFull + i));
