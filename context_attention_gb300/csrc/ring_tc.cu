@@ -539,6 +539,23 @@ __device__ __forceinline__ float exp_row_to_tmem(uint32_t tS, int vis_max, float
   return lo + hi;
 }
 
+// O *= f for this thread's row, out of line: the deferred reference move of
+// the online softmax is rare, and keeping its code out of the hot loop keeps
+// that loop's instructions in the instruction cache.
+__device__ __noinline__ void rescale_o_row(uint32_t tO, float f) {
+#pragma unroll 1
+  for (int ch = 0; ch < kD / 32; ++ch) {
+    uint32_t r[32];
+    tmem_ld32(tO + ch * 32, r);
+    tmem_ld_wait();
+    reg_fence(r);
+#pragma unroll
+    for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * f);
+    tmem_st32(tO + ch * 32, r);
+  }
+  tmem_st_wait();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -805,6 +822,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
       }
       const float c_log2 = c_nat * kLog2e;
       float m = -INFINITY;  // reference max, log2 units (online mode)
+      int pend = 0;         // reference move (log2 units) due before the next tile
       float l = 0.f;
       TileIter it;
       it.begin(P, U);
@@ -825,8 +843,31 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         const int64_t lim = row_lim - (int64_t)it.kt * kBN;
         const int vis_max = (int)max((int64_t)-1, min(lim, (int64_t)(kBN - 1)));
         const bool need_mask = __any_sync(0xffffffffu, vis_max < kBN - 1);
+        // O *= f for this row (online max: the reference moved up)
+        auto rescale_o = [&](float f) {
+#pragma unroll 1
+          for (int ch = 0; ch < kD / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld32(tO + ch * 32, r);
+            tmem_ld_wait();
+            reg_fence(r);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * f);
+            tmem_st32(tO + ch * 32, r);
+          }
+          tmem_st_wait();
+        };
         float mref;
         bool p_done = false;  // P already in TMEM and its sum in l
+        if (!const_max && __any_sync(0xffffffffu, pend > 0)) {
+          // the reference move left by the previous tile (whose PV has
+          // completed: it precedes this tile's S in the MMA order)
+          const float fac = pend > 0 ? __int_as_float((127 - pend) << 23) : 1.f;
+          rescale_o_row(tO, fac);
+          l *= fac;
+          m += (float)pend;
+          pend = 0;
+        }
         if (const_max) {
           mref = c_log2;
         } else if (j > 0 && !__any_sync(0xffffffffu, m == -INFINITY)) {
@@ -837,12 +878,19 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
           uint64_t sum2 = f2_pack(0.f, 0.f);
           const float mx = need_mask ? spec_row<true>(tS, vis_max, sl2_2, nref_2, pk, sum2)
                                      : spec_row<false>(tS, vis_max, sl2_2, nref_2, pk, sum2);
-          if (__all_sync(0xffffffffu, !(mx * P.scale_log2 > m + kRescaleThreshold))) {
+          // how far the tile's maximum lies above the reference.  Up to 64
+          // (log2) this tile's P, l and O stay far from fp32 overflow against
+          // the old reference, so P is kept; past the lazy-rescale threshold
+          // the reference then moves up by a whole number of log2 units
+          // before the next tile (O, l scale by an exact power of two)
+          const float jump = mx * P.scale_log2 - m;
+          if (__all_sync(0xffffffffu, !(jump > 64.f))) {
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) tmem_st16(tS + ch * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * ch]));
             float lo, hi;
             f2_unpack(sum2, lo, hi);
             l += lo + hi;
+            if (jump > kRescaleThreshold) pend = (int)ceilf(jump);  // 9 .. 64
             p_done = true;
           }
           mref = m;
@@ -860,20 +908,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
             l *= fac;
             m = mx;
           }
-          if (__any_sync(0xffffffffu, need_o)) {
-            const float f = need_o ? fac : 1.f;
-#pragma unroll 1
-            for (int ch = 0; ch < kD / 32; ++ch) {
-              uint32_t r[32];
-              tmem_ld32(tO + ch * 32, r);
-              tmem_ld_wait();
-              reg_fence(r);
-#pragma unroll
-              for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * f);
-              tmem_st32(tO + ch * 32, r);
-            }
-            tmem_st_wait();
-          }
+          if (__any_sync(0xffffffffu, need_o)) rescale_o(need_o ? fac : 1.f);
           mref = (m == -INFINITY) ? 0.f : m;
         }
         // pass 2: p = 2^(s*scale*log2e - ref), row sum, bf16 P written over

@@ -249,6 +249,21 @@ def test_const_max_in_kernel_bound_large_scores(ca, dtype, causal, layout):
     assert_close(np32(o2), ro, np32(lse2), rl, dtype=dtype, what=f"kmax {dtype} {layout}")
 
 
+@pytest.mark.parametrize("causal,layout", [(False, "contiguous"), (True, "striped")])
+def test_online_max_large_jumps(ca, causal, layout):
+    """Online max where the row maximum keeps jumping from tile to tile by up
+    to ~245 log2 units (keys of growing norm along the sequence, scores to
+    170 nats): the kernel's reference moves by whole powers of two after a
+    speculative pass, or recomputes the tile when a jump is too large to
+    represent; both must agree with the oracle."""
+    q, k, v = aligned_qk(1, 4, 2, 2048, 128, 16, 48.0, 40.0, torch.float32)
+    ramp = torch.linspace(0.02, 1.0, 2048, device="cuda").view(1, 1, 2048, 1)
+    q, k, v = q.bfloat16(), (k * ramp).bfloat16(), v.bfloat16()
+    ro, rl = oracle_ring(q, k, v, 4, "online_max", causal, layout)
+    o, lse = ca.ring_attn_fwd(q, k, v, 4, mode="online_max", causal=causal, layout=layout)
+    assert_close(np32(o), ro, np32(lse), rl, what=f"online jumps {layout}")
+
+
 def test_const_max_in_kernel_bound_equals_given_bound(ca):
     """The row bound formed in the kernel and the one ca_const_max_bound
     writes agree to fp32 rounding, so the two entry points agree."""
