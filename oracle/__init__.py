@@ -63,6 +63,7 @@ def _load():
             lib.ora_const_max_bound.argtypes = [P, P, I, I, I, I64, I, Dbl, P, P]
             lib.ora_ring_rows.argtypes = [P, P, P, I, I, I, I64, I, Dbl, I, I, I, I, P, P, I64, P, P, P]
             lib.ora_dcp_deal.argtypes = [I64, I, I, P, P]
+            lib.ora_qk_prologue.argtypes = [P, P, Dbl, P, P, I, I64, I, I, I, I, I, P]
             lib.ora_dcp_local_filled.argtypes = [I64, I, I, I]
             lib.ora_dcp_local_filled.restype = I64
             lib.ora_dcp_decode.argtypes = [P, P, P, I, I, I, I64, I, I, I, P, Dbl, P, P]
@@ -77,8 +78,8 @@ def _f32(x) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
 
 
-def _ptr(a: np.ndarray) -> int:
-    return a.ctypes.data
+def _ptr(a):
+    return None if a is None else a.ctypes.data
 
 
 def num_threads() -> int:
@@ -248,3 +249,21 @@ def dcp_decode_paged(q, k_cache, v_cache, block_tables, interleave, seq_lens, sc
     _load().ora_dcp_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), N, Hq, Hkv, nblk, bs, max_blocks,
                                  D, W, int(interleave), _ptr(sl), scale, _ptr(o), _ptr(lse))
     return o, lse
+
+
+def qk_prologue(x, H, g=None, eps=1e-6, cos=None, sin=None, cp=1, layout=LAYOUT_CONTIGUOUS, norm=True):
+    """Attention input [B,H,S,D] (fp64) of one projected tensor x [B,S,H*D]:
+    whole-hidden RMS norm with gain g (norm=True), rotary turn of channel
+    pairs by the per-position tables cos/sin [S, D/2] (if given), rows in the
+    shard-major order of the layout."""
+    x = _f32(x)
+    B, S, HD = x.shape
+    D = HD // H
+    assert H * D == HD and D % 2 == 0 and S % cp == 0
+    gp = None if g is None else _f32(g)
+    cs = None if cos is None else _f32(cos)
+    sn = None if sin is None else _f32(sin)
+    out = np.zeros((B, H, S, D))
+    _load().ora_qk_prologue(_ptr(x), _ptr(gp), float(eps), _ptr(cs), _ptr(sn), B, S, H, D, cp, int(layout),
+                            1 if norm else 0, _ptr(out))
+    return out

@@ -26,6 +26,9 @@
  *    position, then the LSE merge).
  *  - "Sharding the Input" (striped layout: token t on device t mod cp;
  *    causal masking: a later token never influences an earlier one).
+ *  - "Context Parallelism in vLLM Omni Neuron", section "Self-Attention with
+ *    Context Parallelism" (q/k norm over the whole hidden, head split,
+ *    rotary embedding at each token's position).
  *
  * Parity pins: every function here is pinned by the not-gpu tests in
  * tests/test_oracle_pins.py and tests/test_index_maps.py (closed forms,
@@ -532,6 +535,57 @@ void ora_dcp_decode_paged(const float *q, const float *k_cache, const float *v_c
   ora_dcp_decode(q, ks, vs, N, Hq, Hkv, Lloc, D, W, I, seq_lens, scale, o, lse);
   free(ks);
   free(vs);
+}
+
+/* Prologue of const-max attention on one projected tensor: from activations
+ * x [B, S, H*D] in token order (token p at global position p) to the
+ * attention input out [B, H, S, D] in the shard-major row order of `layout`
+ * (stored row rho holds token global_pos(rho)).  "Context Parallelism in
+ * vLLM Omni Neuron", section "Self-Attention with Context Parallelism": the
+ * projected q and k are normalised over the whole hidden before the head
+ * split, then rotary embeddings are applied to every head at the token's
+ * position.
+ *  - norm != 0: y_j = x_j / sqrt(mean over all H*D channels of x^2 + eps)
+ *    * g_j (g == NULL: g_j = 1), the RMS norm of the whole hidden;
+ *    norm == 0: y = x (the value tensor).
+ *  - cs != NULL: every head's channel pairs (2i, 2i+1) turn by the angle of
+ *    token p whose cosine and sine are cs[p*(D/2) + i], sn[p*(D/2) + i]:
+ *      y'_2i = y_2i c - y_2i+1 s,   y'_2i+1 = y_2i s + y_2i+1 c.
+ * All arithmetic in double from the stored (widened) inputs. */
+void ora_qk_prologue(const float *x, const float *g, double eps, const float *cs,
+                     const float *sn, int B, int64_t S, int H, int D, int cp,
+                     int layout, int norm, double *out) {
+  const int64_t Ls = S / cp;
+  const int64_t HD = (int64_t)H * D;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int b = 0; b < B; ++b)
+    for (int64_t rho = 0; rho < S; ++rho) {
+      const int64_t p = global_pos(layout, cp, Ls, rho);
+      const float *xr = x + ((int64_t)b * S + p) * HD;
+      double scale = 1.0;
+      if (norm) {
+        double ss = 0.0;
+        for (int64_t j = 0; j < HD; ++j) ss += (double)xr[j] * (double)xr[j];
+        scale = 1.0 / sqrt(ss / (double)HD + eps);
+      }
+      for (int h = 0; h < H; ++h) {
+        double *o = out + (((int64_t)b * H + h) * S + rho) * D;
+        for (int d = 0; d < D; ++d) {
+          const int64_t j = (int64_t)h * D + d;
+          double y = (double)xr[j];
+          if (norm) y = y * scale * (g ? (double)g[j] : 1.0);
+          o[d] = y;
+        }
+        if (cs) {
+          for (int i = 0; i < D / 2; ++i) {
+            const double c = cs[p * (D / 2) + i], s = sn[p * (D / 2) + i];
+            const double y0 = o[2 * i], y1 = o[2 * i + 1];
+            o[2 * i] = y0 * c - y1 * s;
+            o[2 * i + 1] = y0 * s + y1 * c;
+          }
+        }
+      }
+    }
 }
 
 /* Number of OpenMP threads a parallel region here would use. */

@@ -433,3 +433,86 @@ def test_dcp_decode_paged_equals_contiguous_shards():
     o2, l2 = ora.dcp_decode_paged(q, kc, vc, bt, I, seq_lens)
     np.testing.assert_allclose(o2, o1, atol=1e-12)
     np.testing.assert_allclose(l2, l1, atol=1e-12)
+
+
+# ---------------------------------------------------------------- QK prologue (RMS norm, RoPE, layout)
+
+
+def _rope_tables(S, D, base=10000.0):
+    """Per-position angles p * base^(-2i/D) (one per channel pair)."""
+    ang = np.arange(S)[:, None] * base ** (-2.0 * np.arange(D // 2) / D)[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32), ang
+
+
+def test_prologue_rms_norm_unit_mean_square_and_scale_invariance():
+    """With eps = 0 and no gain every token's normalised hidden has mean
+    square exactly 1, and rescaling a token's activations changes nothing."""
+    B, S, H, D = 2, 6, 3, 8
+    x = rnd(B, S, H * D)
+    out = ora.qk_prologue(x, H, eps=0.0)
+    ms = (out.transpose(0, 2, 1, 3).reshape(B, S, H * D) ** 2).mean(-1)
+    np.testing.assert_allclose(ms, 1.0, atol=1e-12)
+    alpha = np.array([0.25, 4.0, 1e3, 1e-3, 7.0, 0.5])[None, :, None].astype(np.float32)
+    out2 = ora.qk_prologue(x * alpha, H, eps=0.0)
+    np.testing.assert_allclose(out2, out, atol=1e-6)
+
+
+def test_prologue_eps_and_gain_per_channel_of_the_whole_hidden():
+    """A token whose activations are all c: y = c / sqrt(c^2 + eps) * g_j,
+    with the gain indexed by the channel of the whole hidden (h*D + d)."""
+    B, S, H, D = 1, 2, 2, 4
+    x = np.full((B, S, H * D), 0.5, np.float32)
+    g = (1.0 + np.arange(H * D)).astype(np.float32)
+    eps = 0.75
+    out = ora.qk_prologue(x, H, g=g, eps=eps)
+    want = 0.5 / math.sqrt(0.25 + eps) * g.reshape(H, D)
+    for s in range(S):
+        np.testing.assert_allclose(out[0, :, s, :], want, atol=1e-12)
+
+
+def test_prologue_rope_identity_and_quarter_turn():
+    """cos = 1, sin = 0 leaves the normalised values alone; a quarter turn
+    maps each channel pair (y0, y1) of every head to (-y1, y0)."""
+    B, S, H, D = 1, 3, 2, 8
+    x = rnd(B, S, H * D)
+    plain = ora.qk_prologue(x, H)
+    one, zero = np.ones((S, D // 2), np.float32), np.zeros((S, D // 2), np.float32)
+    np.testing.assert_allclose(ora.qk_prologue(x, H, cos=one, sin=zero), plain, atol=1e-15)
+    turned = ora.qk_prologue(x, H, cos=zero, sin=one)
+    np.testing.assert_allclose(turned[..., 0::2], -plain[..., 1::2], atol=1e-15)
+    np.testing.assert_allclose(turned[..., 1::2], plain[..., 0::2], atol=1e-15)
+
+
+def test_prologue_rope_keeps_norms_and_depends_on_relative_position():
+    """Rotation keeps every head's norm; with angles p * w_i the product of a
+    rotated query at m and key at n depends on m - n only."""
+    S, H, D = 12, 1, 16
+    cos, sin, _ = _rope_tables(S, D)
+    u, w = rnd(D), rnd(D)
+    # the same q vector (before norm) at every position; likewise k
+    xq = np.tile(u, (1, S, 1)).astype(np.float32)
+    xk = np.tile(w, (1, S, 1)).astype(np.float32)
+    q = ora.qk_prologue(xq, H, cos=cos, sin=sin, eps=0.0)[0, 0]
+    k = ora.qk_prologue(xk, H, cos=cos, sin=sin, eps=0.0)[0, 0]
+    q0 = ora.qk_prologue(xq, H, eps=0.0)[0, 0]
+    np.testing.assert_allclose(np.linalg.norm(q, axis=-1), np.linalg.norm(q0, axis=-1), rtol=1e-6)
+    for m, n, t in ((3, 1, 5), (0, 7, 4), (9, 9, 2)):
+        np.testing.assert_allclose(q[m] @ k[n], q[m + t] @ k[n + t], atol=1e-5)
+
+
+def test_prologue_striped_rows_hold_the_dealt_tokens():
+    """Striped layout: stored row r*Ls + a of every head holds token a*cp + r
+    (the contiguous output's row), for q-style and value-style tensors."""
+    B, S, H, D, cp = 2, 12, 2, 4, 3
+    x = rnd(B, S, H * D)
+    cos, sin, _ = _rope_tables(S, D)
+    Ls = S // cp
+    for norm in (True, False):
+        cont = ora.qk_prologue(x, H, cos=cos, sin=sin, norm=norm)
+        strp = ora.qk_prologue(x, H, cos=cos, sin=sin, norm=norm, cp=cp, layout=ora.LAYOUT_STRIPED)
+        for r in range(cp):
+            for a in range(Ls):
+                np.testing.assert_array_equal(strp[:, :, r * Ls + a], cont[:, :, a * cp + r])
+    # value-style (no norm, no rope): the plain head split and transpose
+    v = ora.qk_prologue(x, H, norm=False)
+    np.testing.assert_array_equal(v, x.reshape(B, S, H, D).transpose(0, 2, 1, 3))
