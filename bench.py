@@ -396,6 +396,33 @@ def bench_other_workloads(ca, torch, reps=5):
     run("causal GQA striped Hq32 Hkv8 S65536 cp8", q, k, v, 8, "online_max", True, "striped", f)
     del q, k, v
     torch.cuda.empty_cache()
+    # QKV prologue of the DiT workload (B1, S16384, 40 heads of 128, cp8):
+    # whole-hidden RMS norm + gains + rotary turn for q and k, head split for
+    # v, kmax2 of k; HBM bytes = activations read + outputs written + tables
+    B, S, H, D = 1, 16384, 40, 128
+    x_q, x_k, x_v, g_q, g_k, cos, sin = [t.cuda() for t in synth.qkv_activations(B, S, H, H, D, 27)]
+    for _ in range(3):
+        ca.qkv_prologue(x_q, x_k, H, H, x_v=x_v, g_q=g_q, g_k=g_k, rope_cos=cos, rope_sin=sin, cp_size=8)
+    torch.cuda.synchronize()
+    outs = [ca.qkv_prologue(x_q, x_k, H, H, x_v=x_v, g_q=g_q, g_k=g_k, rope_cos=cos, rope_sin=sin, cp_size=8)
+            for _ in range(2)]  # two output sets (> L2 together) so no rep reads the previous one's lines
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(4 * reps):
+        o = outs[i % 2]
+        st = ca._load().ca_qkv_prologue(x_q.data_ptr(), x_k.data_ptr(), x_v.data_ptr(), g_q.data_ptr(),
+                                        g_k.data_ptr(), 1e-6, cos.data_ptr(), sin.data_ptr(), 1, B, S, H, H, D, 8, 0,
+                                        o[0].data_ptr(), o[1].data_ptr(), o[2].data_ptr(), o[3].data_ptr(),
+                                        stream.cuda_stream)
+        assert st == 0, st
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (4 * reps)
+    nbytes = 6 * B * S * H * D * 2 + 2 * S * (D // 2) * 4
+    res["qkv_prologue DiT B1 S16384 H40"] = {"ms": round(ms, 4), "gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
+    del x_q, x_k, x_v, outs
+    torch.cuda.empty_cache()
     # DCP prefill: an 8192-token chunk after 122880 cached tokens, dcp=4, I=16
     Hq, Hkv, W, I, Sc, P = 32, 8, 4, 16, 8192, 122880
     q, kp, vp, kc, vc = synth.dcp_prefill_inputs(Hq, Hkv, 128, W, Sc, P // W, Sc // W, 6, device="cuda")

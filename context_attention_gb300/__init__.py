@@ -74,6 +74,7 @@ def _load():
             "ca_ring_attn_fwd_bounded": ([P, P, P, P, P, P, I, I, I, I, I64, I, I, I, I, F, P], I),
             "ca_ring_attn_fwd_kmax": ([P, P, P, P, P, P, I, I, I, I, I64, I, I, I, I, F, P], I),
             "ca_key_max2": ([P, I, I, I, I64, I, P, P], I),
+            "ca_qkv_prologue": ([P, P, P, P, P, F, P, P, I, I, I64, I, I, I, I, I, P, P, P, P, P], I),
             "ca_attn_partial_step": ([P, P, P, I, I, I, I, I64, I, I, I, I, I, I, I, F, P, P, P, P], I),
             "ca_lse_merge": ([P, P, I, I64, I, P, P, I, P, P], I),
             "ca_const_max_bound": ([P, P, I, I, I, I, I64, I, F, P, P, P], I),
@@ -239,6 +240,29 @@ def lse_merge(o_parts, lse_parts, c=None, out_dtype=torch.float32):
                           _ptr(lse), _stream(o_parts))
     _check("ca_lse_merge", st)
     return o, lse
+
+
+def qkv_prologue(x_q, x_k, Hq, Hkv, x_v=None, g_q=None, g_k=None, eps=1e-6, rope_cos=None, rope_sin=None,
+                 cp_size=1, layout="contiguous", want_kmax2=True):
+    """Attention inputs from projected activations x_q [B,S,Hq*D], x_k (and
+    x_v) [B,S,Hkv*D] (bf16, token order): whole-hidden RMS norm with gains,
+    rotary turn by per-position tables [S, D/2], heads split into [B,H,S,D]
+    in the shard-major row order of the layout.  Returns (q, k, v or None,
+    kmax2 [B,Hkv] or None)."""
+    lib = _load()
+    _need(x_q, "x_q", 3)
+    _need(x_k, "x_k", 3)
+    B, S, HqD = x_q.shape
+    D = HqD // Hq
+    q = torch.empty(B, Hq, S, D, device=x_q.device, dtype=x_q.dtype)
+    k = torch.empty(B, Hkv, S, D, device=x_q.device, dtype=x_q.dtype)
+    v = None if x_v is None else torch.empty(B, Hkv, S, D, device=x_q.device, dtype=x_q.dtype)
+    km = torch.empty(B, Hkv, device=x_q.device, dtype=torch.float32) if want_kmax2 else None
+    st = lib.ca_qkv_prologue(_ptr(x_q), _ptr(x_k), _ptr(x_v), _ptr(g_q), _ptr(g_k), float(eps), _ptr(rope_cos),
+                             _ptr(rope_sin), DTYPE[x_q.dtype], B, S, Hq, Hkv, D, cp_size, LAYOUT[layout], _ptr(q),
+                             _ptr(k), _ptr(v), _ptr(km), _stream(x_q))
+    _check("ca_qkv_prologue", st)
+    return q, k, v, km
 
 
 def key_max2(k, out=None):

@@ -297,6 +297,48 @@ ca_status ca_key_max2(const void* k, ca_dtype dtype, int B, int Hkv, int64_t S, 
                                   static_cast<cudaStream_t>(stream)));
 }
 
+// ------------------------------------------------------------------ prologue
+ca_status ca_qkv_prologue(const void* x_q, const void* x_k, const void* x_v, const float* g_q,
+                          const float* g_k, float eps, const float* rope_cos,
+                          const float* rope_sin, ca_dtype dtype, int B, int64_t S, int Hq,
+                          int Hkv, int D, int cp_size, ca_layout layout, void* q, void* k,
+                          void* v, float* kmax2, void* stream) {
+  if (!x_q || !x_k || !q || !k || (x_v && !v) || (!rope_cos != !rope_sin)) return CA_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || !valid_layout(layout) || B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 ||
+      cp_size <= 0 || !(eps >= 0.f))
+    return CA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || S % cp_size != 0) return CA_ERR_SHAPE;
+  if (dtype != CA_DTYPE_BF16 || (D != 64 && D != 128) || (int64_t)Hq * D > 8192) return CA_ERR_UNSUPPORTED;
+  auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!aligned16(x_q) || !aligned16(x_k) || (x_v && !aligned16(x_v)) || !aligned16(q) ||
+      !aligned16(k) || (v && !aligned16(v)) || (g_q && !aligned16(g_q)) || (g_k && !aligned16(g_k)) ||
+      (rope_cos && (!aligned16(rope_cos) || !aligned16(rope_sin))) || (kmax2 && !a4(kmax2)))
+    return CA_ERR_ALIGNMENT;
+  QkvPrologueArgs a;
+  a.x_q = x_q;
+  a.x_k = x_k;
+  a.x_v = x_v;
+  a.g_q = g_q;
+  a.g_k = g_k;
+  a.eps = eps;
+  a.cos = rope_cos;
+  a.sin = rope_sin;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.S = S;
+  a.cp = cp_size;
+  a.layout = (int)layout;
+  a.q = q;
+  a.k = k;
+  a.v = x_v ? v : nullptr;
+  a.kmax2 = kmax2;
+  a.err = device_error_word();
+  if (!a.err) return CA_ERR_CUDA;
+  return launched(launch_qkv_prologue(a, static_cast<cudaStream_t>(stream)));
+}
+
 // ------------------------------------------------------------------ decode
 size_t ca_dcp_decode_workspace_size(int N, int Hq, int Hkv, int64_t Lloc, int D, int dcp,
                                     int interleave) {

@@ -99,6 +99,29 @@ cudaError_t launch_permute_rows(const void* src, void* dst, int64_t BH, int64_t 
 cudaError_t launch_dcp_shard_rows(const void* src, void* dst, int64_t NH, int64_t L,
                                   int64_t row_bytes, int W, int I, cudaStream_t stream);
 
+// QK(V) prologue of const-max attention: whole-hidden RMS norm + gain +
+// rotary turn for q and k, head split / transpose into the shard layout for
+// q, k, v, and kmax2 of the rounded k.
+struct QkvPrologueArgs {
+  const void* x_q;   // [B, S, Hq*D] bf16
+  const void* x_k;   // [B, S, Hkv*D]
+  const void* x_v;   // [B, S, Hkv*D] or null
+  const float* g_q;  // [Hq*D] or null
+  const float* g_k;  // [Hkv*D] or null
+  float eps;
+  const float* cos;  // [S, D/2] or null
+  const float* sin;
+  int B, Hq, Hkv, D;
+  int64_t S;
+  int cp, layout;
+  void* q;           // [B, Hq, S, D] bf16
+  void* k;           // [B, Hkv, S, D]
+  void* v;           // [B, Hkv, S, D] or null
+  float* kmax2;      // [B, Hkv] or null
+  unsigned* err;     // device error word
+};
+cudaError_t launch_qkv_prologue(const QkvPrologueArgs& a, cudaStream_t stream);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

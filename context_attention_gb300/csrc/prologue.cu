@@ -1,0 +1,305 @@
+// prologue.cu -- the pass that turns projected activations into the inputs
+// of const-max ring attention ("Context Parallelism in vLLM Omni Neuron",
+// section "Self-Attention with Context Parallelism": q and k are normalised
+// over the whole hidden before the head split, rotary embeddings are applied
+// per head at each token's position, and the heads are transposed to
+// [B, H, S, D]), fused with the key half of the const-max bound ("Kernel
+// reference: ring_attention_const_max_fwd", sections "Best practices" and
+// "Transpose prologue with fused norms": the per-head max of |k|^2 is
+// reduced off the tiles the prologue already holds).
+//
+// One warp per token row of one tensor; a warp walks the q, k, v rows of a
+// run of tokens.  Lanes take 16-byte chunks lane, lane + 32, ... (8
+// channels).  A q or k row is read twice: once for its sum of squares and
+// once, moments later (from L1 or L2: HBM sees each row once), for the
+// output, so a lane holds only a few chunks at a time and many warps stay
+// resident to keep loads in flight:
+//   q, k:  y = x * rsqrt(mean(x^2) + eps) * g, then each channel pair
+//          (2i, 2i+1) of a head turns by the token's angle (cos/sin tables
+//          [S, D/2]), rounded to bf16 (packed f32x2 arithmetic);
+//   v:     copied into the head-major layout.
+// The output row of token p is its shard-major row in the chosen layout
+// (contiguous: p; striped: (p mod cp) * S/cp + p div cp).  For k, |k_row|^2
+// of each head is summed from the rounded bf16 values (the ones attention
+// reads), kept as a per-warp running max in shared memory and merged into
+// kmax2[b, h] with one atomicMax per head whenever the warp's tokens move
+// to another batch element.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "index_maps.cuh"
+#include "internal.h"
+
+namespace ca {
+namespace {
+
+constexpr int kWarps = 8;         // per block
+constexpr int kMaxHeads = 128;    // H * D <= 8192 and D >= 64
+
+struct PrologueTensor {
+  const uint4* x;      // [B, S, H*D] bf16
+  const float* g;      // [H*D] or null (gain 1)
+  uint4* out;          // [B, H, S, D] bf16
+  int H;
+  int norm;            // 1: RMS norm + rotation; 0: copy (value)
+  int key;             // 1: reduce |k|^2 per head into kmax2
+};
+
+struct PrologueArgs {
+  PrologueTensor t[3];
+  int ntensors;
+  int B, D;
+  int64_t S;
+  int cp, layout;
+  float eps;
+  const float* cs;     // [S, D/2] or null
+  const float* sn;
+  float* kmax2;        // [B, Hkv] or null
+  int64_t jobs_per_warp;  // tokens per warp
+};
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2u(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// The bf16 pair of a 32-bit word as an fp32 pair (exact).
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
+  return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v) {
+  float lo, hi;
+  f2u(v, lo, hi);
+  return pack2(lo, hi);
+}
+// Sum of squares of the 8 channels of a chunk, as two partial sums.
+__device__ __forceinline__ uint64_t sumsq_chunk(const uint4& u, uint64_t acc) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint64_t v = bf2_to_f2(w[e]);
+    acc = f2fma(v, v, acc);
+  }
+  return acc;
+}
+__device__ __forceinline__ float f2sum(uint64_t v) {
+  float lo, hi;
+  f2u(v, lo, hi);
+  return lo + hi;
+}
+
+constexpr int kGroup = 4;   // chunks per lane in flight per step (output pass)
+constexpr int kGroup1 = 10; // chunks per lane in flight per step (sum-of-squares pass)
+
+__global__ void __launch_bounds__(kWarps * 32, 3)
+prologue_kernel(const PrologueArgs a) {
+  __shared__ float kmx[kWarps][kMaxHeads];
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const int64_t gwarp = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t ntok = (int64_t)a.B * a.S;
+  const int64_t j0 = gwarp * a.jobs_per_warp;
+  const int64_t j1 = min(j0 + a.jobs_per_warp, ntok);
+  const int cph = a.D / 8;  // chunks per head
+  const int64_t Ls = a.S / a.cp;
+  for (int h = lane; h < kMaxHeads; h += 32) kmx[warp][h] = 0.f;
+  __syncwarp();
+  int cur_b = -1;
+  // merge the warp's running key-head maxima of batch element cur_b
+  auto flush = [&]() {
+    if (cur_b >= 0 && a.kmax2) {
+      __syncwarp();
+      for (int h = lane; h < a.t[1].H; h += 32) {
+        // squares are >= 0: float bits order like unsigned integers
+        atomicMax(reinterpret_cast<unsigned*>(a.kmax2) + (int64_t)cur_b * a.t[1].H + h,
+                  __float_as_uint(kmx[warp][h]));
+        kmx[warp][h] = 0.f;
+      }
+      __syncwarp();
+    }
+  };
+  for (int64_t jt = j0 * a.ntensors; jt < j1 * a.ntensors; ++jt) {
+    const int64_t tok = jt / a.ntensors;
+    const int t = (int)(jt % a.ntensors);  // q, k, then v of the token
+    const int b = (int)(tok / a.S);
+    const int64_t p = tok % a.S;  // token (global position)
+    if (b != cur_b) {
+      flush();
+      cur_b = b;
+    }
+    const PrologueTensor& T = a.t[t];
+    const int nchunks = T.H * cph;
+    const int rounds = (nchunks + 31) / 32;
+    const uint4* xr = T.x + tok * nchunks;
+    int r_sh;
+    int64_t a_sh;
+    layout_locate(a.layout, a.cp, Ls, p, &r_sh, &a_sh);
+    const int64_t orow = (int64_t)r_sh * Ls + a_sh;  // stored row of token p
+    uint4* orow_base = T.out + ((int64_t)b * T.H * a.S + orow) * cph;  // head 0 of the row
+    const int64_t head_stride = a.S * cph;                              // uint4 per head
+    if (!T.norm) {
+      for (int i0 = 0; i0 < rounds; i0 += kGroup) {
+        uint4 u[kGroup];
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g) {
+          const int c = lane + 32 * (i0 + g);
+          if (c < nchunks) u[g] = __ldcs(xr + c);  // streamed once
+        }
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g) {
+          const int c = lane + 32 * (i0 + g);
+          if (c < nchunks) orow_base[(c / cph) * head_stride + c % cph] = u[g];
+        }
+      }
+      continue;
+    }
+    // pass 1: sum of squares
+    uint64_t ss2 = f2(0.f, 0.f);
+    for (int i0 = 0; i0 < rounds; i0 += kGroup1) {
+      uint4 u[kGroup1];
+#pragma unroll
+      for (int g = 0; g < kGroup1; ++g) {
+        const int c = lane + 32 * (i0 + g);
+        u[g] = c < nchunks ? __ldg(xr + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int g = 0; g < kGroup1; ++g) ss2 = sumsq_chunk(u[g], ss2);
+    }
+    float ss = f2sum(ss2);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float rstd = rsqrtf(ss / (float)(T.H * a.D) + a.eps);
+    const uint64_t rstd2 = f2(rstd, rstd);
+    const float* cs_row = a.cs ? a.cs + p * (a.D / 2) : nullptr;
+    const float* sn_row = a.cs ? a.sn + p * (a.D / 2) : nullptr;
+    // pass 2: normalise, gain, turn, round, store (and key-head norms)
+    for (int i0 = 0; i0 < rounds; i0 += kGroup) {
+      uint4 u[kGroup];
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        const int c = lane + 32 * (i0 + g);
+        u[g] = c < nchunks ? __ldcs(xr + c) : make_uint4(0, 0, 0, 0);  // last use: evict first
+      }
+      float hsq[kGroup];
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        const int c = lane + 32 * (i0 + g);
+        hsq[g] = 0.f;
+        if (c >= nchunks) continue;
+        const int d0 = (c % cph) * 8;
+        const uint32_t w[4] = {u[g].x, u[g].y, u[g].z, u[g].w};
+        uint64_t y[4];
+        if (T.g) {
+          const float4 g0 = __ldg(reinterpret_cast<const float4*>(T.g + (int64_t)c * 8));
+          const float4 g1 = __ldg(reinterpret_cast<const float4*>(T.g + (int64_t)c * 8 + 4));
+          const uint64_t gg[4] = {f2(g0.x, g0.y), f2(g0.z, g0.w), f2(g1.x, g1.y), f2(g1.z, g1.w)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) y[e] = f2mul(f2mul(bf2_to_f2(w[e]), rstd2), gg[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) y[e] = f2mul(bf2_to_f2(w[e]), rstd2);
+        }
+        if (cs_row) {
+          // (y0, y1) -> (y0 c - y1 s, y0 s + y1 c) = (y0, y1) * c + (-y1, y0) * s
+          const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs_row + d0 / 2));
+          const float4 s4 = __ldg(reinterpret_cast<const float4*>(sn_row + d0 / 2));
+          const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float y0, y1;
+            f2u(y[e], y0, y1);
+            y[e] = f2fma(y[e], f2(cc[e], cc[e]), f2mul(f2(-y1, y0), f2(sv[e], sv[e])));
+          }
+        }
+        const uint4 o = make_uint4(f2_to_bf2(y[0]), f2_to_bf2(y[1]), f2_to_bf2(y[2]), f2_to_bf2(y[3]));
+        orow_base[(c / cph) * head_stride + c % cph] = o;
+        if (T.key) hsq[g] = f2sum(sumsq_chunk(o, f2(0.f, 0.f)));
+      }
+      if (T.key) {
+        // |k|^2 of each head: the cph lanes holding its chunks in a round (32
+        // is a multiple of cph, so heads never straddle rounds); the shuffle
+        // trees of the group's rounds are independent and interleave
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1)
+          if (off < cph) {
+#pragma unroll
+            for (int g = 0; g < kGroup; ++g) hsq[g] += __shfl_xor_sync(0xffffffffu, hsq[g], off, cph);
+          }
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g) {
+          const int c = lane + 32 * (i0 + g);
+          if (c < nchunks && (c % cph) == 0) kmx[warp][c / cph] = fmaxf(kmx[warp][c / cph], hsq[g]);
+        }
+      }
+    }
+  }
+  flush();
+}
+
+}  // namespace
+
+cudaError_t launch_qkv_prologue(const QkvPrologueArgs& q, cudaStream_t stream) {
+  if (q.D != 64 && q.D != 128) return cudaErrorInvalidValue;
+  PrologueArgs a;
+  const void* xs[3] = {q.x_q, q.x_k, q.x_v};
+  const float* gs[3] = {q.g_q, q.g_k, nullptr};
+  void* outs[3] = {q.q, q.k, q.v};
+  const int hs[3] = {q.Hq, q.Hkv, q.Hkv};
+  a.ntensors = 0;
+  int max_h = 0;
+  for (int i = 0; i < 3; ++i) {
+    if (!xs[i]) continue;
+    PrologueTensor& T = a.t[a.ntensors++];
+    T.x = static_cast<const uint4*>(xs[i]);
+    T.g = gs[i];
+    T.out = static_cast<uint4*>(outs[i]);
+    T.H = hs[i];
+    T.norm = i < 2;
+    T.key = i == 1;
+    if (hs[i] > max_h) max_h = hs[i];
+  }
+  if (max_h * q.D > kMaxHeads * 64 || max_h > kMaxHeads) return cudaErrorInvalidValue;
+  a.B = q.B;
+  a.D = q.D;
+  a.S = q.S;
+  a.cp = q.cp;
+  a.layout = q.layout;
+  a.eps = q.eps;
+  a.cs = q.cos;
+  a.sn = q.sin;
+  a.kmax2 = q.kmax2;
+  if (q.kmax2) {
+    cudaError_t e = cudaMemsetAsync(q.kmax2, 0, sizeof(float) * (size_t)q.B * q.Hkv, stream);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t ntok = (int64_t)q.B * q.S;
+  if (ntok == 0) return cudaSuccess;
+  // three blocks (24 warps) resident per SM, each warp with a contiguous run
+  // of tokens
+  const int64_t warps = (int64_t)device_sm_count() * 3 * kWarps;
+  a.jobs_per_warp = (ntok + warps - 1) / warps;
+  const int64_t nwarps = (ntok + a.jobs_per_warp - 1) / a.jobs_per_warp;
+  const unsigned blocks = (unsigned)((nwarps + kWarps - 1) / kWarps);
+  prologue_kernel<<<blocks, kWarps * 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace ca

@@ -18,6 +18,10 @@ Recipes (shapes follow the workloads on the pages on context parallelism):
   picked by a seeded permutation, have their k rows scaled by 8 in every head.
 * ``decode_inputs``: q [N, Hq, D] and interleaved K/V shards
   [W, N, Hkv, Lloc, D], all ~ N(0, 1).
+* ``qkv_activations``: projected activations for the attention prologue:
+  x_q [B, S, Hq*D], x_k, x_v [B, S, Hkv*D] ~ N(0, 1) bf16, per-channel gains
+  1 + 0.1*N(0, 1) (fp32) for q and k, and rotary tables cos/sin [S, D/2] of
+  the angles p * 10000^(-2i/D) (fp32).
 """
 from __future__ import annotations
 
@@ -98,3 +102,23 @@ def dcp_prefill_inputs(Hq, Hkv, D, W, Sc, Lcap, Lc, seed, dtype=torch.bfloat16, 
     kc = torch.randn(W, Hkv, Lc, D, generator=g, device=device).to(dtype)
     vc = torch.randn(W, Hkv, Lc, D, generator=g, device=device).to(dtype)
     return q, kp, vp, kc, vc
+
+
+def rope_tables(S, D, base=10000.0, device="cpu"):
+    """cos, sin [S, D/2] fp32 of the angles p * base^(-2i/D)."""
+    p = torch.arange(S, dtype=torch.float64).view(S, 1)
+    w = base ** (-2.0 * torch.arange(D // 2, dtype=torch.float64) / D)
+    ang = p * w.view(1, -1)
+    return torch.cos(ang).float().to(device), torch.sin(ang).float().to(device)
+
+
+def qkv_activations(B, S, Hq, Hkv, D, seed, device="cpu"):
+    """x_q, x_k, x_v (bf16), g_q, g_k (fp32), cos, sin (fp32); see the module doc."""
+    g = _gen(seed, device)
+    x_q = torch.randn(B, S, Hq * D, generator=g, device=device).to(torch.bfloat16)
+    x_k = torch.randn(B, S, Hkv * D, generator=g, device=device).to(torch.bfloat16)
+    x_v = torch.randn(B, S, Hkv * D, generator=g, device=device).to(torch.bfloat16)
+    g_q = 1.0 + 0.1 * torch.randn(Hq * D, generator=g, device=device)
+    g_k = 1.0 + 0.1 * torch.randn(Hkv * D, generator=g, device=device)
+    cos, sin = rope_tables(S, D, device=device)
+    return x_q, x_k, x_v, g_q, g_k, cos, sin

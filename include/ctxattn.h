@@ -183,6 +183,42 @@ ca_status ca_lse_merge(const float *o_parts, const float *lse_parts, int n,
                        ca_dtype out_dtype, float *lse, void *stream);
 
 /* ------------------------------------------------------------------------
+ * QKV prologue of const-max attention ([CP] "Self-Attention with Context
+ * Parallelism": the projected q and k are normalised over the whole hidden
+ * before the head split and rotary embeddings are applied per head at each
+ * token's position; [CM] "Best practices", "Transpose prologue with fused
+ * norms": the per-head key maximum is reduced in the same pass).  One read
+ * of the activations, one write of the attention inputs:
+ *   q, k:  y_j = x_j / sqrt(mean over the H*D channels of x^2 + eps) * g_j,
+ *          then every head's channel pairs (2i, 2i+1) turn by the token's
+ *          angle: y'_2i = y_2i c - y_2i+1 s, y'_2i+1 = y_2i s + y_2i+1 c with
+ *          c = rope_cos[p*D/2 + i], s = rope_sin[p*D/2 + i]; rounded to bf16;
+ *   v:     split into heads unchanged.
+ * Token p (its global position) lands on row layout-shard-row(p) of every
+ * head of the [B,H,S,D] outputs (contiguous: p; striped: (p mod cp)*S/cp +
+ * p div cp), the row order ca_ring_attn_fwd takes.  kmax2[b,h] = max over the
+ * rows of |k_row|^2 summed in fp32 from the rounded bf16 outputs, ready for
+ * ca_ring_attn_fwd_kmax.
+ *
+ * x_q         device [B,S,Hq*D] bf16 (token order); x_k, x_v [B,S,Hkv*D];
+ *             x_v may be NULL (then v is not written).
+ * g_q, g_k    device [Hq*D] / [Hkv*D] fp32 gains, or NULL (gain 1).
+ * eps         >= 0, added to the mean square.
+ * rope_cos, rope_sin  device [S, D/2] fp32, both or neither (no rotation).
+ * q, k, v     device [B,Hq,S,D] / [B,Hkv,S,D] bf16 outputs.
+ * kmax2       device [B,Hkv] fp32 output (zeroed, then reduced into), or NULL.
+ * All tensor pointers 16-byte aligned (kmax2 4-byte).
+ * Errors: CA_ERR_SHAPE if Hq % Hkv or S % cp_size; CA_ERR_UNSUPPORTED unless
+ * bf16 with D in {64, 128} and Hq*D <= 8192.
+ * ---------------------------------------------------------------------- */
+ca_status ca_qkv_prologue(const void *x_q, const void *x_k, const void *x_v,
+                          const float *g_q, const float *g_k, float eps,
+                          const float *rope_cos, const float *rope_sin,
+                          ca_dtype dtype, int B, int64_t S, int Hq, int Hkv,
+                          int D, int cp_size, ca_layout layout, void *q,
+                          void *k, void *v, float *kmax2, void *stream);
+
+/* ------------------------------------------------------------------------
  * Key maximum of the const-max bound ([CM] "Global key max", "Transpose
  * prologue with fused norms": per head, the running max of |k_j|^2):
  * kmax2[b,hk] = max over the S rows of k[b,hk] of |k_j|^2, squares summed in

@@ -166,3 +166,29 @@ def test_dcp_prefill_validation(ca):
     assert S[pre(kc=FAKE + 8)] == "CA_ERR_ALIGNMENT"
     assert S[lib.ca_dcp_prefill_partial(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 2, 512, 128, 4, 16, 1024, 256, 128, 4,
                                         0.0, FAKE, FAKE, None)] == "CA_ERR_INVALID_ARG"  # rank out of range
+
+
+def test_qkv_prologue_validation(ca):
+    lib = ca._load()
+    S = ca.STATUS
+
+    def pro(**kw):
+        a = dict(xq=FAKE, xk=FAKE, xv=None, gq=None, gk=None, eps=1e-6, cs=None, sn=None, dtype=1, B=1, S=64,
+                 Hq=8, Hkv=2, D=128, cp=4, layout=0, q=FAKE, k=FAKE, v=None, km=None)
+        a.update(kw)
+        return lib.ca_qkv_prologue(a["xq"], a["xk"], a["xv"], a["gq"], a["gk"], a["eps"], a["cs"], a["sn"],
+                                   a["dtype"], a["B"], a["S"], a["Hq"], a["Hkv"], a["D"], a["cp"], a["layout"],
+                                   a["q"], a["k"], a["v"], a["km"], None)
+
+    assert S[pro(xq=None)] == "CA_ERR_INVALID_ARG"
+    assert S[pro(xv=FAKE)] == "CA_ERR_INVALID_ARG"          # x_v without v
+    assert S[pro(cs=FAKE)] == "CA_ERR_INVALID_ARG"          # cos without sin
+    assert S[pro(eps=-1.0)] == "CA_ERR_INVALID_ARG"
+    assert S[pro(layout=5)] == "CA_ERR_INVALID_ARG"
+    assert S[pro(Hq=6, Hkv=4)] == "CA_ERR_SHAPE"
+    assert S[pro(S=66)] == "CA_ERR_SHAPE"                   # S % cp
+    assert S[pro(dtype=0)] == "CA_ERR_UNSUPPORTED"
+    assert S[pro(D=96)] == "CA_ERR_UNSUPPORTED"
+    assert S[pro(Hq=128, Hkv=2)] == "CA_ERR_UNSUPPORTED"    # hidden wider than 8192
+    assert S[pro(k=FAKE + 8)] == "CA_ERR_ALIGNMENT"
+    assert S[pro(km=FAKE + 2)] == "CA_ERR_ALIGNMENT"

@@ -120,3 +120,33 @@ def test_dcp_decode_full(ca):
         assert_close(np32(o[n:n + 1]), ro, np32(lse[n:n + 1]), rl, what=f"decode full n={n}")
     del q, k, v
     torch.cuda.empty_cache()
+
+
+def test_qkv_prologue_dit_full(ca):
+    """The prologue at the DiT workload's size (B=1, S=16384, 40 heads of 128,
+    cp=8) in the benchmark's launch configuration: q, k checked against the
+    oracle on a seeded sample of 512 tokens, v bit-exact everywhere, kmax2
+    against the oracle's key maximum of the written k."""
+    from context_attention_gb300 import synth
+
+    B, S, H, D, cp = 1, 16384, 40, 128, 8
+    x_q, x_k, x_v, g_q, g_k, cos, sin = [t.cuda() for t in synth.qkv_activations(B, S, H, H, D, 26)]
+    q, k, v, km = ca.qkv_prologue(x_q, x_k, H, H, x_v=x_v, g_q=g_q, g_k=g_k, rope_cos=cos, rope_sin=sin,
+                                  cp_size=cp)
+    torch.cuda.synchronize()
+    tok = np.sort(np.random.default_rng(26).choice(S, 512, replace=False))
+    tok = np.unique(np.concatenate([tok, [0, S - 1]]))
+    idx = torch.as_tensor(tok, device="cuda")
+    for x, g, out, what in ((x_q, g_q, q, "q"), (x_k, g_k, k, "k")):
+        # the oracle on the sampled tokens only: rows keep their own tables
+        xs = np32(x.index_select(1, idx))
+        ref = np.zeros((B, H, len(tok), D))
+        for i, t in enumerate(tok):
+            ref[:, :, i:i + 1] = oracle.qk_prologue(xs[:, i:i + 1], H, g=np32(g), eps=1e-6,
+                                                    cos=np32(cos[t:t + 1]), sin=np32(sin[t:t + 1]))
+        gpu = np32(out.index_select(2, idx)).astype(np.float64)  # contiguous layout: row = token
+        err = np.abs(gpu - ref)
+        assert (err <= 2.0 ** -8 * np.abs(ref) + 1e-6).all(), f"{what}: worst {err.max():.3e}"
+    assert torch.equal(v, x_v.view(B, S, H, D).transpose(1, 2))
+    _, rkm = oracle.const_max_bound(np32(k), np32(k))
+    np.testing.assert_allclose(np32(km), rkm, rtol=2e-6)
