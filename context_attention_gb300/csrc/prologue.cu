@@ -110,6 +110,9 @@ __device__ __forceinline__ float f2sum(uint64_t v) {
 constexpr int kGroup = 4;   // chunks per lane in flight per step (output pass)
 constexpr int kGroup1 = 10; // chunks per lane in flight per step (sum-of-squares pass)
 
+// kD: head dimension (64 or 128), a constant so that chunk -> (head, offset)
+// is a shift and a mask.
+template <int kD>
 __global__ void __launch_bounds__(kWarps * 32, 3)
 prologue_kernel(const PrologueArgs a) {
   __shared__ float kmx[kWarps][kMaxHeads];
@@ -118,7 +121,7 @@ prologue_kernel(const PrologueArgs a) {
   const int64_t ntok = (int64_t)a.B * a.S;
   const int64_t j0 = gwarp * a.jobs_per_warp;
   const int64_t j1 = min(j0 + a.jobs_per_warp, ntok);
-  const int cph = a.D / 8;  // chunks per head
+  constexpr int cph = kD / 8;  // chunks per head
   const int64_t Ls = a.S / a.cp;
   for (int h = lane; h < kMaxHeads; h += 32) kmx[warp][h] = 0.f;
   __syncwarp();
@@ -186,10 +189,10 @@ prologue_kernel(const PrologueArgs a) {
     float ss = f2sum(ss2);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    const float rstd = rsqrtf(ss / (float)(T.H * a.D) + a.eps);
+    const float rstd = rsqrtf(ss / (float)(T.H * kD) + a.eps);
     const uint64_t rstd2 = f2(rstd, rstd);
-    const float* cs_row = a.cs ? a.cs + p * (a.D / 2) : nullptr;
-    const float* sn_row = a.cs ? a.sn + p * (a.D / 2) : nullptr;
+    const float* cs_row = a.cs ? a.cs + p * (kD / 2) : nullptr;
+    const float* sn_row = a.cs ? a.sn + p * (kD / 2) : nullptr;
     // pass 2: normalise, gain, turn, round, store (and key-head norms)
     for (int i0 = 0; i0 < rounds; i0 += kGroup) {
       uint4 u[kGroup];
@@ -298,7 +301,10 @@ cudaError_t launch_qkv_prologue(const QkvPrologueArgs& q, cudaStream_t stream) {
   a.jobs_per_warp = (ntok + warps - 1) / warps;
   const int64_t nwarps = (ntok + a.jobs_per_warp - 1) / a.jobs_per_warp;
   const unsigned blocks = (unsigned)((nwarps + kWarps - 1) / kWarps);
-  prologue_kernel<<<blocks, kWarps * 32, 0, stream>>>(a);
+  if (q.D == 128)
+    prologue_kernel<128><<<blocks, kWarps * 32, 0, stream>>>(a);
+  else
+    prologue_kernel<64><<<blocks, kWarps * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
