@@ -309,6 +309,7 @@ ca_status ca_qkv_prologue(const void* x_q, const void* x_k, const void* x_v, con
     return CA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || S % cp_size != 0) return CA_ERR_SHAPE;
   if (dtype != CA_DTYPE_BF16 || (D != 64 && D != 128) || (int64_t)Hq * D > 8192) return CA_ERR_UNSUPPORTED;
+  if ((int64_t)B * S * 3 >= ((int64_t)1 << 31)) return CA_ERR_UNSUPPORTED;  // 32-bit row indices
   auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
   if (!aligned16(x_q) || !aligned16(x_k) || (x_v && !aligned16(x_v)) || !aligned16(q) ||
       !aligned16(k) || (v && !aligned16(v)) || (g_q && !aligned16(g_q)) || (g_k && !aligned16(g_k)) ||

@@ -139,11 +139,17 @@ prologue_kernel(const PrologueArgs a) {
       __syncwarp();
     }
   };
+  // row indices fit 32 bits (the host checks B * S * tensors < 2^31), so the
+  // per-row index arithmetic stays in cheap 32-bit divisions
+  const uint32_t nt = (uint32_t)a.ntensors, S32 = (uint32_t)a.S, cp32 = (uint32_t)a.cp;
   for (int64_t jt = j0 * a.ntensors; jt < j1 * a.ntensors; ++jt) {
-    const int64_t tok = jt / a.ntensors;
-    const int t = (int)(jt % a.ntensors);  // q, k, then v of the token
-    const int b = (int)(tok / a.S);
-    const int64_t p = tok % a.S;  // token (global position)
+    const uint32_t ju = (uint32_t)jt;
+    const uint32_t tok32 = ju / nt;
+    const int t = (int)(ju - tok32 * nt);  // q, k, then v of the token
+    const int b = (int)(tok32 / S32);
+    const uint32_t p32 = tok32 - (uint32_t)b * S32;
+    const int64_t tok = tok32;
+    const int64_t p = p32;  // token (global position)
     if (b != cur_b) {
       flush();
       cur_b = b;
@@ -152,10 +158,12 @@ prologue_kernel(const PrologueArgs a) {
     const int nchunks = T.H * cph;
     const int rounds = (nchunks + 31) / 32;
     const uint4* xr = T.x + tok * nchunks;
-    int r_sh;
-    int64_t a_sh;
-    layout_locate(a.layout, a.cp, Ls, p, &r_sh, &a_sh);
-    const int64_t orow = (int64_t)r_sh * Ls + a_sh;  // stored row of token p
+    // stored row of token p: contiguous p; striped (p mod cp) * Ls + p div cp
+    int64_t orow = p;
+    if (a.layout == kLayoutStriped) {
+      const uint32_t a_sh = p32 / cp32;
+      orow = (int64_t)(p32 - a_sh * cp32) * Ls + a_sh;
+    }
     uint4* orow_base = T.out + ((int64_t)b * T.H * a.S + orow) * cph;  // head 0 of the row
     const int64_t head_stride = a.S * cph;                              // uint4 per head
     if (!T.norm) {

@@ -207,7 +207,7 @@ ca_status ca_lse_merge(const float *o_parts, const float *lse_parts, int n,
  * rope_cos, rope_sin  device [S, D/2] fp32, both or neither (no rotation).
  * q, k, v     device [B,Hq,S,D] / [B,Hkv,S,D] bf16 outputs.
  * kmax2       device [B,Hkv] fp32 output (zeroed, then reduced into), or NULL.
- * All tensor pointers 16-byte aligned (kmax2 4-byte).
+ * All tensor pointers 16-byte aligned (kmax2 4-byte); B*S*3 < 2^31.
  * Errors: CA_ERR_SHAPE if Hq % Hkv or S % cp_size; CA_ERR_UNSUPPORTED unless
  * bf16 with D in {64, 128} and Hq*D <= 8192.
  * ---------------------------------------------------------------------- */

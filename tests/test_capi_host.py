@@ -190,5 +190,6 @@ def test_qkv_prologue_validation(ca):
     assert S[pro(dtype=0)] == "CA_ERR_UNSUPPORTED"
     assert S[pro(D=96)] == "CA_ERR_UNSUPPORTED"
     assert S[pro(Hq=128, Hkv=2)] == "CA_ERR_UNSUPPORTED"    # hidden wider than 8192
+    assert S[pro(S=1 << 30, cp=1)] == "CA_ERR_UNSUPPORTED"  # rows past 32-bit indices
     assert S[pro(k=FAKE + 8)] == "CA_ERR_ALIGNMENT"
     assert S[pro(km=FAKE + 2)] == "CA_ERR_ALIGNMENT"
