@@ -556,6 +556,9 @@ __device__ __noinline__ void rescale_o_row(uint32_t tO, float f) {
   tmem_st_wait();
 }
 
+// kConst: the const-max instantiation (no running maximum) or the online-max
+// one; each compiles only its own softmax.
+template <bool kConst>
 __global__ void __launch_bounds__(kThreads, 1)
 ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -758,7 +761,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_base + kColS + 128u * i;
     const uint32_t tO = tmem + lane_base + kColO + 128u * i;
-    const bool const_max = P.a.mode == 1;
+    constexpr bool const_max = kConst;
     // Softmax warpgroup 1's first thread releases the K/V ring slots and the
     // Q tiles: the issuing thread commits s_full[1] after S1(j), which it
     // issues after S0(j), PV0(j-1) and PV1(j-1), so once s_full[1] of tile j
@@ -1014,20 +1017,25 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
 
 }  // namespace
 
-static cudaError_t launch_tc(const TcMaps& maps, const TcParams& P, cudaStream_t stream) {
+template <bool kConst>
+static cudaError_t launch_tc_mode(const TcMaps& maps, const TcParams& P, cudaStream_t stream) {
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(ring_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemAlloc);
+    cudaError_t e = cudaFuncSetAttribute(ring_tc_kernel<kConst>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
   const int sms = device_sm_count();
   const int64_t grid = P.units < sms ? P.units : sms;
-  ring_tc_kernel<<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(maps, P);
+  ring_tc_kernel<kConst><<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(maps, P);
   return cudaGetLastError();
+}
+
+static cudaError_t launch_tc(const TcMaps& maps, const TcParams& P, cudaStream_t stream) {
+  return P.a.mode == 1 ? launch_tc_mode<true>(maps, P, stream) : launch_tc_mode<false>(maps, P, stream);
 }
 
 static void init_common(TcParams& P, const RingArgs& a) {
