@@ -498,6 +498,13 @@ def run_profile_case(args):
         km = ca.key_max2(k)
         for _ in range(args.warmup + 1):
             ca.ring_attn_fwd_kmax(q, k, v, km, PREFILL["cp"])
+    elif args.profile == "prologue":
+        # the DiT prologue (B1 S16384 40 heads): 1 GB moved per launch (> L2), ~0.2 ms
+        B, S, H, D = 1, PREFILL["S"], PREFILL["H"], PREFILL["D"]
+        x_q, x_k, x_v, g_q, g_k, cos, sin = [t.cuda() for t in synth.qkv_activations(B, S, H, H, D, 27)]
+        for _ in range(args.warmup + 1):
+            ca.qkv_prologue(x_q, x_k, H, H, x_v=x_v, g_q=g_q, g_k=g_k, rope_cos=cos, rope_sin=sin,
+                            cp_size=PREFILL["cp"])
     else:
         # decode recipe with 4 sequences: K+V 2.1 GB (> L2), one launch ~0.3 ms
         d = DECODE
@@ -636,7 +643,7 @@ def main():
                     help="also time the online-max, sink and causal GQA workloads (reported, not the value)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--profile", choices=["ring", "decode"], default=None,
+    ap.add_argument("--profile", choices=["ring", "decode", "prologue"], default=None,
                     help="run one small launch of one kernel (for ncu captures) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
