@@ -159,16 +159,18 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       const int32_t* bt = a.block_tables + ((int64_t)I.r * a.N + I.n) * a.max_blocks;
       for (int st = 0; st < nst; ++st) {
         const int slot = (int)(pos % kStages);
-        ok = __all_sync(0xffffffffu, mbar_wait(empty(slot), (uint32_t)(((pos / kStages) & 1) ^ 1),
-                                               abort_flag, err));
-        if (!ok) break;
         const int64_t first = I.t0 + (int64_t)st * kTok;  // first local slot of the stage
         const int64_t nvalid = min((int64_t)kTok, I.ntok - (int64_t)st * kTok);
         const int nb = (int)((nvalid + a.bs - 1) / a.bs);
+        // the stage's block ids, read before waiting for the slot so that
+        // their latency overlaps the wait
+        const int64_t blk = lane < nb ? (int64_t)__ldg(bt + first / a.bs + lane) : 0;
+        ok = __all_sync(0xffffffffu, mbar_wait(empty(slot), (uint32_t)(((pos / kStages) & 1) ^ 1),
+                                               abort_flag, err));
+        if (!ok) break;
         if (lane == 0) mbar_arrive_expect_tx(full(slot), (uint32_t)nb * 4 * box_bytes);
         __syncwarp();
         if (lane < nb) {
-          const int64_t blk = bt[first / a.bs + lane];
           const int row = (int)((((int64_t)I.r * a.nblk + blk) * a.Hkv + I.hkv) * a.bs);
           const uint32_t dst = sbase + kSmemStages + slot * kStageBytes + (uint32_t)lane * box_bytes;
           tma_load_2d_hint(dst + 0 * kBox, &tk, full(slot), 0, row, policy);
