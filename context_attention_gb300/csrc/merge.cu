@@ -21,7 +21,6 @@ namespace ca {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
-constexpr int kMaxChunks = 4;  // float4 chunks per lane: D <= 512
 
 __device__ __forceinline__ float warp_max(float x) {
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
@@ -32,6 +31,8 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// kMaxChunks: float4 chunks per lane (D <= 128 * kMaxChunks).
+template <int kMaxChunks>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ lse_parts, int n,
                  int64_t R, int D, const float* __restrict__ c, void* __restrict__ o, int out_bf16,
@@ -75,25 +76,38 @@ lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ ls
 #pragma unroll
   for (int j = 0; j < kMaxChunks; ++j) sum[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (!empty) {
-    for (int i = 0; i < n; ++i) {
-      const float li = lse_parts[(int64_t)i * R + row];
-      float w;
-      if (c) {
-        w = 1.f;  // pure addition of unnormalised sums
-      } else {
-        if (li == -INFINITY) continue;
-        w = expf(li - out_lse);
+    // partials in groups of 32: lane l holds the weight of partial g + l;
+    // the rows of kUnroll partials are loaded before any is accumulated
+    constexpr int kUnroll = 8;
+    for (int g = 0; g < n; g += 32) {
+      float wl = 0.f;
+      if (g + lane < n) {
+        const float li = lse_parts[(int64_t)(g + lane) * R + row];
+        // const max: pure addition of unnormalised sums
+        wl = c ? 1.f : (li == -INFINITY ? 0.f : expf(li - out_lse));
       }
-      const float4* src = reinterpret_cast<const float4*>(o_parts + ((int64_t)i * R + row) * D);
+      const int m = min(32, n - g);
+      for (int i0 = 0; i0 < m; i0 += kUnroll) {
+        float4 x[kUnroll][kMaxChunks];
 #pragma unroll
-      for (int j = 0; j < kMaxChunks; ++j) {
-        const int ch = lane + 32 * j;
-        if (ch < nch) {
-          const float4 x = __ldg(src + ch);
-          sum[j].x = fmaf(w, x.x, sum[j].x);
-          sum[j].y = fmaf(w, x.y, sum[j].y);
-          sum[j].z = fmaf(w, x.z, sum[j].z);
-          sum[j].w = fmaf(w, x.w, sum[j].w);
+        for (int u = 0; u < kUnroll; ++u) {
+          const float4* src = reinterpret_cast<const float4*>(o_parts + ((int64_t)(g + i0 + u) * R + row) * D);
+#pragma unroll
+          for (int j = 0; j < kMaxChunks; ++j) {
+            const int ch = lane + 32 * j;
+            x[u][j] = (i0 + u < m && ch < nch) ? __ldg(src + ch) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const float w = __shfl_sync(0xffffffffu, wl, (i0 + u) & 31);
+#pragma unroll
+          for (int j = 0; j < kMaxChunks; ++j) {
+            sum[j].x = fmaf(w, x[u][j].x, sum[j].x);
+            sum[j].y = fmaf(w, x[u][j].y, sum[j].y);
+            sum[j].z = fmaf(w, x[u][j].z, sum[j].z);
+            sum[j].w = fmaf(w, x[u][j].w, sum[j].w);
+          }
         }
       }
     }
@@ -128,8 +142,13 @@ cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int n
                              cudaStream_t stream) {
   if (R == 0) return cudaSuccess;
   const int64_t blocks = (R + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  lse_merge_kernel<<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(o_parts, lse_parts, n, R,
-                                                                        D, c, o, out_bf16, lse);
+  const unsigned g = (unsigned)blocks, t = kWarpsPerBlock * 32;
+  if (D <= 128)
+    lse_merge_kernel<1><<<g, t, 0, stream>>>(o_parts, lse_parts, n, R, D, c, o, out_bf16, lse);
+  else if (D <= 256)
+    lse_merge_kernel<2><<<g, t, 0, stream>>>(o_parts, lse_parts, n, R, D, c, o, out_bf16, lse);
+  else
+    lse_merge_kernel<4><<<g, t, 0, stream>>>(o_parts, lse_parts, n, R, D, c, o, out_bf16, lse);
   return cudaGetLastError();
 }
 
