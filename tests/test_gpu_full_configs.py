@@ -150,3 +150,37 @@ def test_qkv_prologue_dit_full(ca):
     assert torch.equal(v, x_v.view(B, S, H, D).transpose(1, 2))
     _, rkm = oracle.const_max_bound(np32(k), np32(k))
     np.testing.assert_allclose(np32(km), rkm, rtol=2e-6)
+
+
+@pytest.mark.parametrize("mode,causal,layout", [("online_max", True, "striped"), ("const_max", False, "contiguous")])
+def test_long_context_one_million_tokens(ca, mode, causal, layout):
+    """S = 2^20 tokens (one head pair, GQA 2:1, cp = 8: 131072-token
+    shards), so row indices, TMA coordinates and tile counts run far past
+    the benchmark sizes; sampled rows (every shard's first and last row)
+    against the oracle."""
+    from context_attention_gb300 import synth
+
+    S = 1 << 20
+    q, k, v = synth.normal_qkv(1, 2, 1, S, 128, 61, dtype=torch.bfloat16, device="cuda")
+    sampled_parity(ca, q, k, v, 8, mode, causal, layout, [(0, 0), (0, 1)], 24, 62,
+                   f"1M tokens {mode} {layout}")
+    del q, k, v
+    torch.cuda.empty_cache()
+
+
+def test_dcp_decode_one_million_token_context(ca):
+    """One sequence with a 1M-token context over dcp = 4 shards of 262144
+    slots (4 GB of K and V), full and roughly half length; the decode must
+    stream every valid slot once and merge to the oracle's result."""
+    from context_attention_gb300 import synth
+
+    N, Hq, Hkv, W, I, Lloc = 1, 32, 8, 4, 16, 1 << 18
+    q, k, v = synth.decode_inputs(N, Hq, Hkv, 128, W, Lloc, 63, device="cuda")
+    for L in (W * Lloc, W * Lloc // 2 + 40):
+        sl = torch.tensor([L], dtype=torch.int32, device="cuda")
+        o, lse = ca.dcp_decode(q, k, v, I, seq_lens=sl)
+        torch.cuda.synchronize()
+        ro, rl = oracle.dcp_decode(np32(q), np32(k), np32(v), I, seq_lens=np.array([L]))
+        assert_close(np32(o), ro, np32(lse), rl, what=f"decode 1M context L={L}")
+    del q, k, v
+    torch.cuda.empty_cache()
