@@ -18,8 +18,11 @@ import threading
 import torch
 
 __all__ = [
-    "CtxAttnError", "build", "library_path", "ring_attn_fwd", "ring_attn_fwd_bounded", "attn_partial_step", "lse_merge",
-    "const_max_bound", "dcp_decode", "dcp_decode_noalloc", "dcp_decode_paged", "paged_kv_write", "dcp_prefill", "dcp_prefill_partial", "layout_to_shards", "layout_from_shards", "dcp_shard_kv",
+    "CtxAttnError", "build", "library_path",
+    "ring_attn_fwd", "ring_attn_fwd_bounded", "ring_attn_fwd_kmax", "attn_partial_step", "lse_merge",
+    "qkv_prologue", "key_max2", "const_max_bound",
+    "dcp_decode", "dcp_decode_noalloc", "dcp_decode_paged", "paged_kv_write", "dcp_prefill", "dcp_prefill_partial",
+    "layout_to_shards", "layout_from_shards", "dcp_shard_kv",
     "layout_global_index", "layout_shard_row", "ring_kv_shard", "dcp_owner", "dcp_local_index",
     "dcp_local_to_global", "dcp_local_filled", "dcp_active_mask", "dcp_slot_mapping",
     "device_status", "ring_attn_fwd_workspace_size", "dcp_decode_workspace_size",
