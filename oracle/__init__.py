@@ -68,6 +68,7 @@ def _load():
             lib.ora_dcp_local_filled.restype = I64
             lib.ora_dcp_decode.argtypes = [P, P, P, I, I, I, I64, I, I, I, P, Dbl, P, P]
             lib.ora_dcp_prefill.argtypes = [P, P, P, P, P, I, I, I64, I, I, I, I64, I64, I64, Dbl, I, P, I64, P, P]
+            lib.ora_ring_decode.argtypes = [P, P, P, I, I, I, I64, I, I, I, P, Dbl, P, P]
             lib.ora_dcp_decode_paged.argtypes = [P, P, P, P, I, I, I, I64, I, I64, I, I, I, P, Dbl, P, P]
             lib.ora_num_threads.restype = I
             _lib = lib
@@ -207,6 +208,25 @@ def dcp_decode(q, k_shards, v_shards, interleave, seq_lens=None, scale=None):
     lse = np.zeros((N, Hq))
     _load().ora_dcp_decode(_ptr(q), _ptr(k_shards), _ptr(v_shards), N, Hq, Hkv, Lloc, D, W,
                            int(interleave), _ptr(sl), scale, _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def ring_decode(q, k, v, cp, layout=LAYOUT_CONTIGUOUS, seq_lens=None, scale=None):
+    """Ring Pass-Q decode over the ring layout's cache.  q [B,Hq,D]; k/v
+    [B,Hkv,S,D] shard-major; seq_lens [B] (default S).  Returns (o, lse)."""
+    q = _f32(q)
+    k, v = _f32(k), _f32(v)
+    B, Hq, D = q.shape
+    Bk, Hkv, S, Dk = k.shape
+    assert Bk == B and Dk == D and Hq % Hkv == 0 and S % cp == 0
+    if seq_lens is None:
+        seq_lens = np.full(B, S, dtype=np.int64)
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int64))
+    scale = 1.0 / np.sqrt(D) if scale is None else float(scale)
+    o = np.zeros((B, Hq, D))
+    lse = np.zeros((B, Hq))
+    _load().ora_ring_decode(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, S, D, int(cp), int(layout), _ptr(sl), scale,
+                            _ptr(o), _ptr(lse))
     return o, lse
 
 

@@ -25,7 +25,9 @@
  *    chunked prefill against prior + current local KV, causal by global
  *    position, then the LSE merge).
  *  - "Sharding the Input" (striped layout: token t on device t mod cp;
- *    causal masking: a later token never influences an earlier one).
+ *    causal masking: a later token never influences an earlier one; Ring
+ *    Pass-Q decode: the query visits the shards of the cache, partials are
+ *    merged).
  *  - "Context Parallelism in vLLM Omni Neuron", section "Self-Attention with
  *    Context Parallelism" (q/k norm over the whole hidden, head split,
  *    rotary embedding at each token's position).
@@ -398,6 +400,61 @@ void ora_dcp_decode(const float *q, const float *k_shards,
     ora_lse_merge(op, lp, W, 1, D, o + nh * D, lse + nh);
     free(own);
     free(loc);
+    free(op);
+    free(lp);
+  }
+}
+
+/* Ring Pass-Q decode ("Sharding the Input", its paragraph on the decode
+ * phase): the KV cache stays where the sharded prefill left it and the single
+ * query token of each sequence visits every shard, which computes a partial
+ * attention over its own part of the cache; the partials are merged by their
+ * log-sum-exp.  The cache is the ring layout: k, v [B, Hkv, S, D], each head's
+ * S rows shard-major (row rho = r*Ls + a is local token a of shard r, at the
+ * global position global_pos gives).  Sequence b's query attends to the
+ * global positions [0, seq_lens[b]), all visible (it is the next token).
+ * Shard r's partial covers its rows whose global position is below
+ * seq_lens[b] (none: lse_r = -inf); the cp partials are LSE-merged.
+ * q [B, Hq, D]; o [B, Hq, D], lse [B, Hq]. */
+void ora_ring_decode(const float *q, const float *k, const float *v, int B, int Hq, int Hkv,
+                     int64_t S, int D, int cp, int layout, const int64_t *seq_lens,
+                     double scale, double *o, double *lse) {
+  int G = Hq / Hkv;
+  int64_t Ls = S / cp;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bh = 0; bh < (int64_t)B * Hq; ++bh) {
+    int64_t b = bh / Hq, h = bh % Hq, hk = h / G;
+    int64_t L = seq_lens[b];
+    const float *qrow = q + bh * D;
+    const float *kh = k + ((int64_t)b * Hkv + hk) * S * D;
+    const float *vh = v + ((int64_t)b * Hkv + hk) * S * D;
+    double *op = (double *)calloc((size_t)cp * D, sizeof(double));
+    double *lp = (double *)malloc(sizeof(double) * (size_t)cp);
+    for (int r = 0; r < cp; ++r) {
+      double m = -INFINITY;
+      for (int64_t rho = r * Ls; rho < (r + 1) * Ls; ++rho) {
+        if (global_pos(layout, cp, Ls, rho) >= L) continue;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += (double)qrow[d] * (double)kh[rho * D + d];
+        if (scale * dot > m) m = scale * dot;
+      }
+      if (m == -INFINITY) {
+        lp[r] = -INFINITY;
+        continue;
+      }
+      double l = 0.0;
+      for (int64_t rho = r * Ls; rho < (r + 1) * Ls; ++rho) {
+        if (global_pos(layout, cp, Ls, rho) >= L) continue;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += (double)qrow[d] * (double)kh[rho * D + d];
+        double w = exp(scale * dot - m);
+        l += w;
+        for (int d = 0; d < D; ++d) op[(int64_t)r * D + d] += w * (double)vh[rho * D + d];
+      }
+      for (int d = 0; d < D; ++d) op[(int64_t)r * D + d] /= l;
+      lp[r] = m + log(l);
+    }
+    ora_lse_merge(op, lp, cp, 1, D, o + bh * D, lse + bh);
     free(op);
     free(lp);
   }

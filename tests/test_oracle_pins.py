@@ -343,6 +343,68 @@ def test_dcp_decode_zero_query_closed_form():
         np.testing.assert_allclose(lse[n], math.log(seq_lens[n]), atol=1e-12)
 
 
+# ---------------------------------------------------------------- ring Pass-Q decode
+
+
+def _ring_cache(kg, cp, layout):
+    """Store a global-order cache [B, Hkv, S, D] in the ring layout by dealing
+    tokens as "Sharding the Input" describes: contiguous blocks of S/cp tokens
+    per shard, or (striped) token t to shard t mod cp as its (t div cp)-th."""
+    B, Hkv, S, D = kg.shape
+    Ls = S // cp
+    out = np.empty_like(kg)
+    for t in range(S):
+        r, a = (t // Ls, t % Ls) if layout == ora.LAYOUT_CONTIGUOUS else (t % cp, t // cp)
+        out[:, :, r * Ls + a] = kg[:, :, t]
+    return out
+
+
+@pytest.mark.parametrize("layout", [ora.LAYOUT_CONTIGUOUS, ora.LAYOUT_STRIPED])
+def test_ring_decode_equals_attention_over_the_prefix(layout):
+    """Pass-Q decode over the ring layout's shards = plain attention of the
+    query over global positions [0, seq_len); cache slots at or past seq_len
+    hold junk that must not be read."""
+    B, Hq, Hkv, D, cp, S = 3, 4, 2, 8, 4, 48
+    q = rnd(B, Hq, D)
+    kg, vg = rnd(B, Hkv, S, D), rnd(B, Hkv, S, D)
+    seq_lens = np.array([48, 29, 1])
+    kj, vj = kg.copy(), vg.copy()
+    for b in range(B):
+        kj[b, :, seq_lens[b]:] = 1e3
+        vj[b, :, seq_lens[b]:] = -1e3
+    k, v = _ring_cache(kj, cp, layout), _ring_cache(vj, cp, layout)
+    o, lse = ora.ring_decode(q, k, v, cp, layout, seq_lens=seq_lens)
+    for b in range(B):
+        Lb = seq_lens[b]
+        qfull = np.zeros((1, Hq, Lb, D), np.float32)
+        qfull[0, :, 0] = q[b]
+        o_ref, l_ref = ora.attention(qfull, kg[b, :, :Lb][None], vg[b, :, :Lb][None], rows=[h * Lb for h in range(Hq)])
+        np.testing.assert_allclose(o[b], o_ref, atol=1e-12)
+        np.testing.assert_allclose(lse[b], l_ref, atol=1e-12)
+
+
+def test_ring_decode_closed_forms():
+    """q = 0: the mean of the visible values and lse = ln(seq_len); one
+    visible token: its value and lse = scale q.k; no visible token: o = 0,
+    lse = -inf."""
+    B, Hq, Hkv, D, cp, S = 3, 2, 1, 4, 8, 64
+    kg, vg = rnd(B, Hkv, S, D), rnd(B, Hkv, S, D)
+    for layout in (ora.LAYOUT_CONTIGUOUS, ora.LAYOUT_STRIPED):
+        k, v = _ring_cache(kg, cp, layout), _ring_cache(vg, cp, layout)
+        seq_lens = np.array([64, 21, 3])
+        o, lse = ora.ring_decode(np.zeros((B, Hq, D), np.float32), k, v, cp, layout, seq_lens=seq_lens)
+        for b in range(B):
+            mean = vg[b, 0, : seq_lens[b]].astype(np.float64).mean(0)
+            np.testing.assert_allclose(o[b], np.broadcast_to(mean, (Hq, D)), atol=1e-12)
+            np.testing.assert_allclose(lse[b], math.log(seq_lens[b]), atol=1e-12)
+        q = rnd(B, Hq, D)
+        o, lse = ora.ring_decode(q, k, v, cp, layout, seq_lens=np.array([1, 1, 0]), scale=0.25)
+        for b in range(2):
+            np.testing.assert_allclose(o[b], np.broadcast_to(vg[b, 0, 0].astype(np.float64), (Hq, D)), atol=1e-12)
+            np.testing.assert_allclose(lse[b], 0.25 * q[b].astype(np.float64) @ kg[b, 0, 0].astype(np.float64), atol=1e-12)
+        assert np.all(o[2] == 0.0) and np.all(np.isneginf(lse[2]))
+
+
 # ---------------------------------------------------------------- DCP prefill
 
 
