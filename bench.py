@@ -476,6 +476,29 @@ def bench_other_workloads(ca, torch, reps=5):
                                                         "gbs": round(decode_bytes() / (ms / 1e3) / 1e9, 1)}
     del q, kc, vc, bt
     torch.cuda.empty_cache()
+    # Ring Pass-Q decode: the decode workload's sequences and 34 GB of K/V,
+    # held in the ring prefill's layout ([B, Hkv, S, D], striped over 8 shards)
+    S = d["W"] * d["Lloc"]
+    q = torch.randn(d["N"], d["Hq"], d["D"], generator=g, device="cuda").to(torch.bfloat16)
+    kr = torch.empty(d["N"], d["Hkv"], S, d["D"], device="cuda", dtype=torch.bfloat16)
+    vr = torch.empty_like(kr)
+    for t in (kr, vr):
+        for n in range(d["N"]):
+            t[n].copy_(torch.randn(d["Hkv"], S, d["D"], generator=g, device="cuda").to(torch.bfloat16))
+    ws = torch.empty(ca.ring_decode_workspace_size(d["N"], d["Hq"], d["Hkv"], S, d["D"], 8), dtype=torch.uint8,
+                     device="cuda")
+    for _ in range(3):
+        ca.ring_decode(q, kr, vr, 8, layout="striped", out=out, lse=lse, workspace=ws)
+    a.record(stream)
+    for _ in range(reps):
+        ca.ring_decode(q, kr, vr, 8, layout="striped", out=out, lse=lse, workspace=ws)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    res["ring_decode striped cp8 64seqs L131072"] = {"ms": round(ms, 3),
+                                                     "gbs": round(decode_bytes() / (ms / 1e3) / 1e9, 1)}
+    del q, kr, vr
+    torch.cuda.empty_cache()
     return res
 
 

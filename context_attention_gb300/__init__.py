@@ -21,11 +21,11 @@ __all__ = [
     "CtxAttnError", "build", "library_path",
     "ring_attn_fwd", "ring_attn_fwd_bounded", "ring_attn_fwd_kmax", "attn_partial_step", "lse_merge",
     "qkv_prologue", "key_max2", "const_max_bound",
-    "dcp_decode", "dcp_decode_noalloc", "dcp_decode_paged", "paged_kv_write", "dcp_prefill", "dcp_prefill_partial",
+    "ring_decode", "dcp_decode", "dcp_decode_noalloc", "dcp_decode_paged", "paged_kv_write", "dcp_prefill", "dcp_prefill_partial",
     "layout_to_shards", "layout_from_shards", "dcp_shard_kv",
     "layout_global_index", "layout_shard_row", "ring_kv_shard", "dcp_owner", "dcp_local_index",
     "dcp_local_to_global", "dcp_local_filled", "dcp_active_mask", "dcp_slot_mapping",
-    "device_status", "ring_attn_fwd_workspace_size", "dcp_decode_workspace_size",
+    "device_status", "ring_attn_fwd_workspace_size", "dcp_decode_workspace_size", "ring_decode_workspace_size",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -84,6 +84,8 @@ def _load():
             "ca_dcp_decode_workspace_size": ([I, I, I, I64, I, I, I], SZ),
             "ca_dcp_decode": ([P, P, P, I, I, I, I, I64, I, I, I, P, F, P, P, P, SZ, P], I),
             "ca_dcp_decode_noalloc": ([P, P, P, I, I, I, I, I64, I, I, I, P, F, P, P, P], I),
+            "ca_ring_decode_workspace_size": ([I, I, I, I64, I, I], SZ),
+            "ca_ring_decode": ([P, P, P, I, I, I, I, I64, I, I, I, P, F, P, P, P, SZ, P], I),
             "ca_dcp_decode_paged": ([P, P, P, P, I, I, I, I, I64, I, I64, I, I, I, P, F, P, P, P, SZ, P], I),
             "ca_paged_kv_write": ([P, P, P, P, P, I, I, I, I, I, I64, I, P], I),
             "ca_dcp_prefill": ([P, P, P, P, P, I, I, I, I64, I, I, I, I64, I64, I64, F, P, P, P], I),
@@ -295,6 +297,11 @@ def const_max_bound(q, k, softmax_scale=None):
     return c, kmax2
 
 
+def ring_decode_workspace_size(B, Hq, Hkv, S, D, cp_size):
+    """Workspace bytes of ring_decode (its split-KV partials)."""
+    return int(_load().ca_ring_decode_workspace_size(B, Hq, Hkv, S, D, cp_size))
+
+
 def dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, dcp, interleave) -> int:
     return int(_load().ca_dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, dcp, interleave))
 
@@ -324,6 +331,36 @@ def dcp_decode(q, k_shards, v_shards, interleave, seq_lens=None, softmax_scale=N
                            D, W, interleave, _ptr(seq_lens), float(softmax_scale or 0.0), _ptr(out),
                            _ptr(lse), _ptr(workspace), workspace.numel(), _stream(q))
     _check("ca_dcp_decode", st)
+    return out, lse
+
+
+def ring_decode(q, k, v, cp_size, layout="contiguous", seq_lens=None, softmax_scale=None, out=None, lse=None,
+                workspace=None):
+    """Ring Pass-Q decode: one query token per sequence over the ring layout's
+    KV cache.  q [B,Hq,D]; k/v [B,Hkv,S,D] shard-major (bf16, D=128).
+
+    seq_lens: optional CUDA int32 [B] (cached tokens, default S).  Returns
+    (o [B,Hq,D], lse [B,Hq])."""
+    lib = _load()
+    _need(q, "q", 3)
+    _need(k, "k", 4)
+    _need(v, "v", 4)
+    B, Hq, D = q.shape
+    _, Hkv, S, _ = k.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, device=q.device, dtype=torch.float32)
+    ws_bytes = int(lib.ca_ring_decode_workspace_size(B, Hq, Hkv, S, D, cp_size))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), device=q.device, dtype=torch.uint8)
+    if seq_lens is not None:
+        if not (seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()):
+            raise ValueError("seq_lens must be a contiguous CUDA int32 tensor")
+    st = lib.ca_ring_decode(_ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, Hq, Hkv, S, D, cp_size, LAYOUT[layout],
+                            _ptr(seq_lens), float(softmax_scale or 0.0), _ptr(out), _ptr(lse), _ptr(workspace),
+                            workspace.numel(), _stream(q))
+    _check("ca_ring_decode", st)
     return out, lse
 
 

@@ -404,6 +404,70 @@ ca_status ca_dcp_decode(const void* q, const void* k_shards, const void* v_shard
                                    o, 1, lse, s));
 }
 
+size_t ca_ring_decode_workspace_size(int B, int Hq, int Hkv, int64_t S, int D, int cp_size) {
+  (void)Hkv;
+  if (B <= 0 || Hq <= 0 || S <= 0 || D <= 0 || cp_size <= 0 || S % cp_size != 0) return 0;
+  int64_t chunk;
+  int splits;
+  dcp_decode_split(S / cp_size, &chunk, &splits);
+  const size_t parts = (size_t)cp_size * splits;
+  return align256(sizeof(float) * parts * B * Hq * D) + align256(sizeof(float) * parts * B * Hq);
+}
+
+ca_status ca_ring_decode(const void* q, const void* k, const void* v, ca_dtype dtype, int B, int Hq,
+                         int Hkv, int64_t S, int D, int cp_size, ca_layout layout,
+                         const int32_t* seq_lens, float softmax_scale, void* o, float* lse,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o) return CA_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || !valid_layout(layout) || B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 ||
+      D <= 0 || cp_size <= 0)
+    return CA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || S % cp_size != 0) return CA_ERR_SHAPE;
+  if (dtype != CA_DTYPE_BF16 || D != 128 || Hq / Hkv > 8) return CA_ERR_UNSUPPORTED;
+  if ((int64_t)B * Hkv * S >= ((int64_t)1 << 31)) return CA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
+      (seq_lens && (reinterpret_cast<uintptr_t>(seq_lens) & 3u)))
+    return CA_ERR_ALIGNMENT;
+  const size_t need = ca_ring_decode_workspace_size(B, Hq, Hkv, S, D, cp_size);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return CA_ERR_WORKSPACE;
+  ca_status st = device_is_gb300();
+  if (st != CA_OK) return st;
+  unsigned* err = device_error_word();
+  if (!err) return CA_ERR_CUDA;
+  // the decode kernel over the ring layout: sequence n = batch element b,
+  // W = cp shards of Lloc = S/cp rows each
+  DecodeArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.N = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.W = cp_size;
+  a.I = 1;
+  a.Lloc = S / cp_size;
+  a.seq_lens = seq_lens;
+  a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
+  dcp_decode_split(a.Lloc, &a.chunk, &a.splits);
+  const size_t parts = (size_t)cp_size * a.splits;
+  a.o_parts = static_cast<float*>(workspace);
+  a.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         align256(sizeof(float) * parts * B * Hq * D));
+  a.err = err;
+  a.paged = 0;
+  a.block_tables = nullptr;
+  a.nblk = a.max_blocks = 0;
+  a.bs = 0;
+  a.ring_layout = (int)layout;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_dcp_decode_partials(a, s);
+  if (e != cudaSuccess) return launched(e);
+  return launched(launch_lse_merge(a.o_parts, a.lse_parts, (int)parts, (int64_t)B * Hq, D, nullptr,
+                                   o, 1, lse, s));
+}
+
 ca_status ca_dcp_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* block_tables, ca_dtype dtype, int N, int Hq, int Hkv,
                               int64_t nblk, int block_size, int64_t max_blocks, int D, int dcp,

@@ -1,4 +1,6 @@
-// decode.cu -- split-KV decode over interleaved DCP shards.
+// decode.cu -- split-KV decode over interleaved DCP shards, and over the ring
+// layout's shards (Ring Pass-Q decode, "Sharding the Input": the KV cache stays
+// where the sharded prefill put it and the query visits every shard).
 //
 // "DCP (Decode Context Parallelism)", section "Decode Compute Pattern": the
 // gathered query heads of a sequence attend to each rank's local KV shard and
@@ -7,16 +9,18 @@
 // many local slots of rank r hold tokens of a sequence of length N; every one
 // of them is visible to the decoded token (its own K/V sits on its owner).
 //
-// One GPU holds all dcp shards.  A work item is (rank r, sequence n, KV head,
-// split of the rank's valid slots).  The scan is HBM bound: a TMA producer
-// warp streams 128-token stages (K and V, 64 KB) through a 3-stage ring; four
-// consumer warps each take 32 tokens of a stage.  The G query heads that
-// share a KV head are the N side of warp-level bf16 MMAs (m16n8k16, fp32
-// accumulate): S^T = K Q^T per 16 tokens, then O^T += V^T P^T, with P moved
-// from the accumulator layout to the operand layout by movmatrix.  Row maxima
-// use the same lazy rescale as the prefill kernel (threshold 2^8).  At the end
-// of an item the four warps' partial states are LSE-merged in shared memory
-// and one partial (o, lse) per query head is written.
+// One GPU holds all shards (dcp ranks, or the cp shards of the ring layout,
+// whose valid slots and rows differ only in item_of).  A work item is (shard
+// r, sequence n, KV head, split of the shard's valid slots).  The scan is HBM
+// bound: a TMA producer warp streams 128-token stages (K and V, 64 KB) through
+// a 3-stage ring; four consumer warps each take 32 tokens of a stage.  The G
+// query heads that share a KV head are the N side of warp-level bf16 MMAs
+// (m16n8k16, fp32 accumulate): S^T = K Q^T per 16 tokens, then O^T += V^T P^T,
+// with P moved from the accumulator layout to the operand layout by
+// movmatrix.  Row maxima use the same lazy rescale as the prefill kernel
+// (threshold 2^8).  At the end of an item the four warps' partial states are
+// LSE-merged in shared memory and one partial (o, lse) per query head is
+// written.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -99,13 +103,15 @@ __device__ __forceinline__ Item item_of(const DecParams& P, int64_t it) {
   I.n = (int)(rest % a.N);
   I.r = (int)(rest / a.N);
   const int64_t seq = a.seq_lens ? (int64_t)a.seq_lens[I.n] : (int64_t)a.W * a.Lloc;
-  int64_t valid = dcp_local_filled(seq, a.W, a.I, a.I, I.r);
+  int64_t valid = a.ring_layout < 0 ? dcp_local_filled(seq, a.W, a.I, a.I, I.r)
+                                    : ring_shard_filled(seq, a.W, a.Lloc, a.ring_layout, I.r);
   if (valid > a.Lloc) valid = a.Lloc;
   I.t0 = (int64_t)I.split * a.chunk;
   I.ntok = valid - I.t0;
   if (I.ntok > a.chunk) I.ntok = a.chunk;
   if (I.ntok < 0) I.ntok = 0;
-  I.row0 = (((int64_t)I.r * a.N + I.n) * a.Hkv + I.hkv) * a.Lloc + I.t0;
+  I.row0 = a.ring_layout < 0 ? (((int64_t)I.r * a.N + I.n) * a.Hkv + I.hkv) * a.Lloc + I.t0
+                              : (((int64_t)I.n * a.Hkv + I.hkv) * a.W + I.r) * a.Lloc + I.t0;
   return I;
 }
 

@@ -87,6 +87,20 @@ CA_HD int64_t dcp_local_filled(int64_t N, int W, int I, int block_size, int R) {
   return filled + extra;
 }
 
+// Slots of ring-layout shard r (Ls rows) that hold one of the global
+// positions [0, N): contiguous shard r holds [r*Ls, (r+1)*Ls); striped shard
+// r holds r, r + cp, r + 2 cp, ... ("Sharding the Input").
+CA_HD int64_t ring_shard_filled(int64_t N, int cp, int64_t Ls, int layout, int r) {
+  int64_t n;
+  if (layout == kLayoutStriped)
+    n = N > r ? (N - r + cp - 1) / cp : 0;
+  else
+    n = N - (int64_t)r * Ls;
+  if (n < 0) n = 0;
+  if (n > Ls) n = Ls;
+  return n;
+}
+
 // dcp_active_mask as the DCP page prints it.
 CA_HD int dcp_active_mask(int64_t N, int W, int I, int block_size, int R) {
   const int64_t vblock = (int64_t)block_size * W;

@@ -84,6 +84,9 @@ struct DecodeArgs {
   const int32_t* block_tables;  // [W, N, max_blocks]
   int64_t nblk, max_blocks;
   int bs;
+  // -1: DCP shards [W, N, Hkv, Lloc, D] (interleave I); kLayoutContiguous or
+  // kLayoutStriped: the ring layout [N, Hkv, W*Lloc, D], shard-major rows
+  int ring_layout = -1;
 };
 cudaError_t launch_dcp_decode_partials(const DecodeArgs& a, cudaStream_t stream);
 // Decode split geometry shared by the workspace query and the launch.

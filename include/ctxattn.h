@@ -297,6 +297,38 @@ ca_status ca_dcp_decode_noalloc(const void *q, const void *k_shards,
                                 void *stream);
 
 /* ------------------------------------------------------------------------
+ * Ring Pass-Q decode ([SHI], its paragraph on the decode phase): the KV
+ * cache stays in the ring layout the sharded prefill left it in and the one
+ * query token of each sequence visits every shard; shard r computes a
+ * partial (o_r, lse_r) over its slots that hold one of the global positions
+ * [0, seq_len) -- all of them visible, the query being the next token -- and
+ * the cp partials are LSE-merged ([DCP] "Decode Compute Pattern").  On one
+ * GPU the query's "visits" are work items of one kernel; no data moves.
+ *
+ * q           device [B, Hq, D], dtype (one query token per sequence).
+ * k, v        device [B, Hkv, S, D], dtype, each head's rows shard-major as
+ *             in ca_ring_attn_fwd: row r*Ls + a is local token a of shard r,
+ *             at global position r*Ls + a (CA_LAYOUT_CONTIGUOUS) or a*cp + r
+ *             (CA_LAYOUT_STRIPED).  Slots at global positions >= seq_len are
+ *             never read.
+ * seq_lens    device int32 [B] (tokens in the cache, 0..S), or NULL for S.
+ * o           device [B, Hq, D], dtype; lse device [B, Hq] fp32 (or NULL).
+ *             A sequence with seq_len 0 gets o = 0, lse = -inf.
+ * workspace   device, ca_ring_decode_workspace_size() bytes (partials).
+ * Errors: CA_ERR_SHAPE if Hq % Hkv != 0 or S % cp_size != 0;
+ * CA_ERR_UNSUPPORTED unless bf16 with D = 128, Hq/Hkv <= 8 and
+ * B*Hkv*S < 2^31.
+ * ---------------------------------------------------------------------- */
+size_t ca_ring_decode_workspace_size(int B, int Hq, int Hkv, int64_t S, int D,
+                                     int cp_size);
+ca_status ca_ring_decode(const void *q, const void *k, const void *v,
+                         ca_dtype dtype, int B, int Hq, int Hkv, int64_t S,
+                         int D, int cp_size, ca_layout layout,
+                         const int32_t *seq_lens, float softmax_scale, void *o,
+                         float *lse, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* ------------------------------------------------------------------------
  * DCP decode over paged KV caches ([DCP] "Slot Mapping and KV Cache",
  * "Segmented Attention CP" step 1: KV read from the cache through the block
  * table).  Same computation as ca_dcp_decode; rank r's local slot s of

@@ -139,6 +139,30 @@ def test_merge_bound_decode_layout_validation(ca):
     assert S[dec(ws_bytes=16)] == "CA_ERR_WORKSPACE"
     assert lib.ca_dcp_decode_workspace_size(64, 32, 8, 32768, 128, 4, 16) > 64 * 32 * 128 * 4 * 4
 
+    def rdec(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=1, B=2, Hq=8, Hkv=2, S=1024, D=128, cp=4, layout=0, seq=None,
+                 scale=0.0, o=FAKE, lse=FAKE, ws=FAKE, ws_bytes=1 << 30, stream=None)
+        a.update(kw)
+        return lib.ca_ring_decode(a["q"], a["k"], a["v"], a["dtype"], a["B"], a["Hq"], a["Hkv"], a["S"], a["D"],
+                                  a["cp"], a["layout"], a["seq"], a["scale"], a["o"], a["lse"], a["ws"],
+                                  a["ws_bytes"], a["stream"])
+
+    assert S[rdec(S=1022)] == "CA_ERR_SHAPE"            # S % cp_size
+    assert S[rdec(Hq=6, Hkv=4)] == "CA_ERR_SHAPE"
+    assert S[rdec(layout=2)] == "CA_ERR_INVALID_ARG"
+    assert S[rdec(v=None)] == "CA_ERR_INVALID_ARG"
+    assert S[rdec(dtype=0)] == "CA_ERR_UNSUPPORTED"
+    assert S[rdec(D=64)] == "CA_ERR_UNSUPPORTED"
+    assert S[rdec(Hq=32, Hkv=2)] == "CA_ERR_UNSUPPORTED"  # more than 8 query heads per KV head
+    assert S[rdec(B=1 << 12, Hkv=8, Hq=8, S=1 << 16)] == "CA_ERR_UNSUPPORTED"  # 2^31 cache rows
+    assert S[rdec(k=FAKE + 8)] == "CA_ERR_ALIGNMENT"
+    assert S[rdec(ws=None)] == "CA_ERR_WORKSPACE"
+    assert S[rdec(ws_bytes=16)] == "CA_ERR_WORKSPACE"
+    # cp partials (each shard split like a DCP rank's slots) of every (sequence, head)
+    assert lib.ca_ring_decode_workspace_size(2, 8, 2, 1024, 128, 4) == lib.ca_dcp_decode_workspace_size(
+        2, 8, 2, 256, 128, 4, 16)
+    assert lib.ca_ring_decode_workspace_size(2, 8, 2, 1022, 128, 4) == 0
+
     assert S[lib.ca_layout_to_shards(FAKE, FAKE, 2, 100, 256, 8, 0, None)] == "CA_ERR_SHAPE"
     assert S[lib.ca_layout_to_shards(FAKE, FAKE, 2, 64, 100, 8, 0, None)] == "CA_ERR_UNSUPPORTED"
     assert S[lib.ca_dcp_shard_kv(FAKE, FAKE, 2, 100, 256, 4, 16, None)] == "CA_ERR_SHAPE"
