@@ -279,7 +279,14 @@ def bench_prefill(ca, torch, steps, warmup, pg, dev_index):
         return start.elapsed_time(end)
 
     run_e2e(3)
-    e2e_steps = max(4, min(steps, 20))
+    # the host link drops to about a third of its copy bandwidth after a
+    # second or two without copies (the device-only timed loop before this)
+    # and takes a few hundred milliseconds of traffic to come back: keep the
+    # copies going for half a second before the timed steps
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < 0.5:
+        run_e2e(10)
+    e2e_steps = max(4, min(steps, 40))
     res["e2e_ms"] = run_e2e(e2e_steps) / e2e_steps
     res["h2d_bytes"] = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
     res["d2h_bytes"] = ohs[0].numel() * ohs[0].element_size()
