@@ -363,6 +363,18 @@ class OracleSampler:
                     f"{t:.1f} s on {threads} threads", seconds=t)
 
 
+def causal_rank_imbalance(S, cp, layout):
+    """Max over mean of the causal work per virtual rank if each rank ran its
+    own queries (a multi-GPU ring): rank r's queries sit at the global
+    positions of its shard, and query p sees the p + 1 keys 0..p."""
+    import numpy as np
+
+    Ls = S // cp
+    a = np.arange(Ls, dtype=np.float64)
+    work = [float(np.sum((r * Ls + a if layout == "contiguous" else a * cp + r) + 1)) for r in range(cp)]
+    return round(max(work) / (sum(work) / cp), 4)
+
+
 def bench_other_workloads(ca, torch, reps=5):
     """Device time of the other ring-attention workloads (online max, sink
     keys, causal GQA in both layouts) with the same CUDA-event method; each
@@ -399,8 +411,10 @@ def bench_other_workloads(ca, torch, reps=5):
     del q, k, v
     q, k, v = synth.normal_qkv(1, 32, 8, 65536, 128, 4, dtype=torch.bfloat16, device="cuda")
     f = 4.0 * 32 * 128 * 65536 * 65537 / 2
-    run("causal GQA contiguous Hq32 Hkv8 S65536 cp8", q, k, v, 8, "online_max", True, "contiguous", f)
-    run("causal GQA striped Hq32 Hkv8 S65536 cp8", q, k, v, 8, "online_max", True, "striped", f)
+    for layout in ("contiguous", "striped"):
+        name = f"causal GQA {layout} Hq32 Hkv8 S65536 cp8"
+        run(name, q, k, v, 8, "online_max", True, layout, f)
+        res[name]["virtual_rank_imbalance"] = causal_rank_imbalance(65536, 8, layout)
     del q, k, v
     torch.cuda.empty_cache()
     # QKV prologue of the DiT workload (B1, S16384, 40 heads of 128, cp8):
