@@ -36,17 +36,24 @@ def assert_close(gpu_o, ref_o, gpu_lse=None, ref_lse=None, dtype=torch.bfloat16,
 
 
 def sample_rows(B, H, S, cp, n_per_head, seed, heads=None):
-    """Seeded sample of (b, h, rho) rows: every shard's first and last row,
-    plus random rows; returns {(b, h): sorted rho array}."""
+    """Seeded sample of (b, h, rho) rows: every shard's first and last row and
+    the rows on both sides of its first 128-row tile boundary (where causal
+    diagonal tiles start and end), plus random rows; returns
+    {(b, h): sorted rho array}."""
     rng = np.random.default_rng(seed)
     Ls = S // cp
     out = {}
     pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
     for b, h in pairs:
-        fixed = [r * Ls for r in range(cp)] + [r * Ls + Ls - 1 for r in range(cp)]
+        fixed = [r * Ls + a for r in range(cp) for a in (0, 127, 128, Ls - 1) if a < Ls]
         rnd = rng.integers(0, S, size=max(0, n_per_head - len(fixed)))
         out[(b, h)] = np.unique(np.concatenate([fixed, rnd]).astype(np.int64))
     return out
+
+
+def rows_per_head(B, H, total=4096):
+    """Rows per (b, h) so that a sample over every head holds >= total rows."""
+    return -(-total // (B * H))
 
 
 def oracle_ring_sampled(q, k, v, cp, rows_by_head, mode, causal=False, layout=0, scale=None, c_full=None):

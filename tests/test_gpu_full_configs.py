@@ -1,12 +1,16 @@
 """Parity at the full workload sizes, in the launch configuration the
 benchmark times, on seeded samples of output rows that the oracle computes
-one by one (every shard's first and last row plus random rows)."""
+one by one: at least 4096 rows per configuration over every (batch, head),
+every shard's first and last row and its first tile boundary, plus random
+rows; and one comparison of every row of the DiT workload."""
+import time
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from helpers import assert_close, np32, oracle_ring_sampled, sample_rows
+from helpers import assert_close, np32, oracle_ring_sampled, rows_per_head, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -49,10 +53,37 @@ def test_dit_const_max_full(ca):
     from context_attention_gb300 import synth
 
     q, k, v = synth.dit_qk(1, 40, 16384, 128, seed=2, device="cuda")
-    heads = [(0, h) for h in (0, 13, 27, 39)]
     for mode in ("const_max", "online_max"):
-        sampled_parity(ca, q, k, v, 8, mode, False, "contiguous", heads, 40, 21, f"dit {mode}")
+        sampled_parity(ca, q, k, v, 8, mode, False, "contiguous", None, rows_per_head(1, 40), 21, f"dit {mode}")
     del q, k, v
+    torch.cuda.empty_cache()
+
+
+def test_dit_const_max_every_row(ca):
+    """Every one of the DiT workload's 655360 output rows (const max, the
+    benchmark's launch) against the oracle; the oracle's time for the whole
+    run is printed beside the rate the CPU baseline extrapolates from a
+    sample (rows are independent, so the two should agree)."""
+    from context_attention_gb300 import synth
+
+    B, H, S, D, cp = 1, 40, 16384, 128, 8
+    q, k, v = synth.dit_qk(B, H, S, D, seed=2, device="cuda")
+    kmax2 = ca.key_max2(k)
+    o, lse = ca.ring_attn_fwd_kmax(q, k, v, kmax2, cp)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    worst = 0.0
+    for h in range(H):
+        qq, kk, vv = np32(q[:, h:h + 1]), np32(k[:, h:h + 1]), np32(v[:, h:h + 1])
+        cc, _ = oracle.const_max_bound(qq, kk)
+        ro, rl, _ = oracle.ring(qq, kk, vv, cp, mode=oracle.MODE_CONST_MAX, c=cc)
+        err, _ = assert_close(np32(o[:, h:h + 1]), ro, np32(lse[:, h:h + 1]), rl, what=f"dit every row h={h}")
+        worst = max(worst, err)
+    dt = time.perf_counter() - t0
+    tflops = 4.0 * H * S * S * D / dt / 1e12
+    print(f"\nfull DiT oracle run: {dt:.1f} s on {oracle.num_threads()} threads = {tflops:.4f} TFLOP/s; "
+          f"worst max-abs error {worst:.3e}")
+    del q, k, v, o, lse
     torch.cuda.empty_cache()
 
 
@@ -64,11 +95,12 @@ def test_online_max_full_and_sinks(ca):
     from context_attention_gb300 import synth
 
     q, k, v = synth.normal_qkv(2, 32, 32, 32768, 128, 3, dtype=torch.bfloat16, device="cuda")
-    heads = [(0, 0), (1, 31)]
-    sampled_parity(ca, q, k, v, 8, "online_max", False, "contiguous", heads, 40, 31, "online N(0,1)")
+    n = rows_per_head(2, 32)
+    sampled_parity(ca, q, k, v, 8, "online_max", False, "contiguous", None, n, 31, "online N(0,1)")
     rows_sink = synth.sink_rows(2, 32768, seed=33, device="cuda")
     k = synth.apply_sinks(k, rows_sink)
-    sampled_parity(ca, q, k, v, 8, "online_max", False, "contiguous", heads, 40, 32, "online sinks")
+    sampled_parity(ca, q, k, v, 8, "online_max", False, "contiguous", None, n, 32, "online sinks")
+    heads = [(0, 0), (1, 31)]
     # const max on the sink variant: a diagnostic of the documented failure
     B, H, S, _ = q.shape
     rows = sample_rows(B, H, S, 8, 60, 34, heads=heads)
@@ -100,8 +132,7 @@ def test_causal_gqa_full(ca, layout):
     from context_attention_gb300 import synth
 
     q, k, v = synth.normal_qkv(1, 32, 8, 65536, 128, 4, dtype=torch.bfloat16, device="cuda")
-    heads = [(0, 0), (0, 5), (0, 31)]
-    sampled_parity(ca, q, k, v, 8, "online_max", True, layout, heads, 30, 41, f"causal {layout}")
+    sampled_parity(ca, q, k, v, 8, "online_max", True, layout, None, rows_per_head(1, 32), 41, f"causal {layout}")
     del q, k, v
     torch.cuda.empty_cache()
 
