@@ -11,9 +11,9 @@
 // One warp per token row of one tensor; a warp walks the q, k, v rows of a
 // run of tokens.  Each warp streams its rows through a few shared-memory
 // buffers of its own with 1-D bulk copies (cp.async.bulk, completing on one
-// mbarrier per buffer), so whole rows are in flight while the previous one
-// is processed, and both passes over a q or k row read shared memory: HBM
-// sees each input byte once and the load pipe stays full with few warps.
+// mbarrier per buffer), so whole rows are in flight while other rows are
+// processed, and both passes over a q or k row read shared memory: HBM sees
+// each input byte once and the load pipe stays full with few warps.
 // Lanes take 16-byte chunks lane, lane + 32, ... (8 channels):
 //   q, k:  y = x * rsqrt(mean(x^2) + eps) * g, then each channel pair
 //          (2i, 2i+1) of a head turns by the token's angle (cos/sin tables
@@ -352,11 +352,13 @@ cudaError_t launch_qkv_prologue(const QkvPrologueArgs& q, cudaStream_t stream) {
   if (ntok == 0) return cudaSuccess;
   a.err = q.err;
   // one block per SM; buffers sized for the longest row, as many warps as
-  // shared memory holds with two buffers each (more buffers for short rows,
-  // so that a warp keeps about 16 KB or more in flight)
+  // shared memory holds.  Long rows get one buffer per warp (the next row is
+  // requested as soon as the current one has been read): more warps, each
+  // with one row in flight, outrun fewer warps that prefetch deeper.  Short
+  // rows get more buffers, so that a warp keeps about 8 KB or more in flight.
   const uint32_t row_bytes = (uint32_t)max_h * q.D * 2;
   a.buf_bytes = (row_bytes + 127) / 128 * 128;
-  a.nbuf = a.buf_bytes >= 8192 ? 2 : a.buf_bytes >= 4096 ? 3 : kMaxBufs;
+  a.nbuf = a.buf_bytes >= 8192 ? 1 : a.buf_bytes >= 4096 ? 2 : kMaxBufs;
   constexpr uint32_t kSmemBudget = 232448;  // per block, opt-in maximum
   a.gain_floats = (uint32_t)((q.g_q ? q.Hq : 0) + (q.g_k ? q.Hkv : 0)) * q.D;
   const uint32_t gain_bytes = (a.gain_floats * 4 + 127) / 128 * 128;
