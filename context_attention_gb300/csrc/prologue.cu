@@ -60,7 +60,7 @@ struct PrologueArgs {
   const float* sn;
   float* kmax2;        // [B, Hkv] or null
   int64_t jobs_per_warp;  // tokens per warp
-  int nbuf;            // row buffers per warp (2..kMaxBufs)
+  int nbuf;            // row buffers per warp (1..kMaxBufs)
   uint32_t buf_bytes;  // bytes per buffer (>= the longest row, multiple of 128)
   uint32_t gain_floats;  // gains staged in shared memory (q's then k's)
   unsigned* err;       // device error word
