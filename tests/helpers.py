@@ -35,6 +35,26 @@ def assert_close(gpu_o, ref_o, gpu_lse=None, ref_lse=None, dtype=torch.bfloat16,
     return err.max(), err.mean()
 
 
+def parity_report(what, gpu_o, ref_o, gpu_lse, ref_lse, oracle_s):
+    """Print one line of parity figures (rows compared, max / mean abs error
+    of o, max abs error of the finite lse, oracle seconds); run pytest with
+    -s to see them."""
+    ref_o = np.asarray(ref_o)
+    g = np.asarray(gpu_o, dtype=np.float64).reshape(ref_o.shape)
+    err = np.abs(g - ref_o)
+    rl = np.asarray(ref_lse, dtype=np.float64).reshape(-1)
+    gl = np.asarray(gpu_lse, dtype=np.float64).reshape(-1)
+    fin = np.isfinite(rl)
+    le = float(np.abs(gl[fin] - rl[fin]).max()) if fin.any() else 0.0
+    at = np.unravel_index(int(np.argmax(err)), err.shape)
+    # half a bf16 ulp of the exact value at the worst element: the output
+    # rounding alone, part of every bf16 result's error
+    half_ulp = 2.0 ** (np.floor(np.log2(max(abs(float(ref_o[at])), 1e-30))) - 8)
+    print(f"\nPARITY {what}: rows={rl.size} max_abs={err.max():.3e} mean_abs={err.mean():.3e} "
+          f"lse_abs={le:.3e} oracle_s={oracle_s:.1f} |o| at worst={abs(float(ref_o[at])):.3f} "
+          f"(bf16 half-ulp {half_ulp:.2e})", flush=True)
+
+
 def sample_rows(B, H, S, cp, n_per_head, seed, heads=None):
     """Seeded sample of (b, h, rho) rows: every shard's first and last row and
     the rows on both sides of its first 128-row tile boundary (where causal

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import assert_close, np32, oracle_ring_sampled, rows_per_head, sample_rows
+from helpers import assert_close, np32, oracle_ring_sampled, parity_report, rows_per_head, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -24,7 +24,7 @@ def ca(cuda_device):
     assert m.device_status() == 0, "a bounded device wait gave up"
 
 
-def check_sampled(o, lse, rows, ref, what):
+def check_sampled(o, lse, rows, ref, what, oracle_s=0.0):
     gpu_o, gpu_l, ref_o, ref_l = [], [], [], []
     for (b, h), (ro, rl, _) in ref.items():
         idx = torch.as_tensor(rows[(b, h)], device=o.device)
@@ -34,6 +34,8 @@ def check_sampled(o, lse, rows, ref, what):
         ref_l.append(rl)
     assert_close(np.concatenate(gpu_o), np.concatenate(ref_o), np.concatenate(gpu_l), np.concatenate(ref_l),
                  what=what)
+    parity_report(what, np.concatenate(gpu_o), np.concatenate(ref_o), np.concatenate(gpu_l), np.concatenate(ref_l),
+                  oracle_s)
 
 
 def sampled_parity(ca, q, k, v, cp, mode, causal, layout, heads, n_rows, seed, what):
@@ -41,9 +43,10 @@ def sampled_parity(ca, q, k, v, cp, mode, causal, layout, heads, n_rows, seed, w
     rows = sample_rows(B, H, S, cp, n_rows, seed, heads=heads)
     o, lse = ca.ring_attn_fwd(q, k, v, cp, mode=mode, causal=causal, layout=layout)
     torch.cuda.synchronize()
+    t0 = time.perf_counter()
     ref = oracle_ring_sampled(q, k, v, cp, rows, oracle.MODE_CONST_MAX if mode == "const_max" else 0,
                               causal=causal, layout=1 if layout == "striped" else 0)
-    check_sampled(o, lse, rows, ref, what)
+    check_sampled(o, lse, rows, ref, what, time.perf_counter() - t0)
     return o, lse, ref
 
 
@@ -72,17 +75,20 @@ def test_dit_const_max_every_row(ca):
     o, lse = ca.ring_attn_fwd_kmax(q, k, v, kmax2, cp)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    worst = 0.0
+    worst, err_sum, lse_worst = 0.0, 0.0, 0.0
     for h in range(H):
         qq, kk, vv = np32(q[:, h:h + 1]), np32(k[:, h:h + 1]), np32(v[:, h:h + 1])
         cc, _ = oracle.const_max_bound(qq, kk)
         ro, rl, _ = oracle.ring(qq, kk, vv, cp, mode=oracle.MODE_CONST_MAX, c=cc)
-        err, _ = assert_close(np32(o[:, h:h + 1]), ro, np32(lse[:, h:h + 1]), rl, what=f"dit every row h={h}")
+        err, mean = assert_close(np32(o[:, h:h + 1]), ro, np32(lse[:, h:h + 1]), rl, what=f"dit every row h={h}")
         worst = max(worst, err)
+        err_sum += mean
+        lse_worst = max(lse_worst, float(np.abs(np32(lse[:, h:h + 1]).reshape(-1) - np.asarray(rl).reshape(-1)).max()))
     dt = time.perf_counter() - t0
     tflops = 4.0 * H * S * S * D / dt / 1e12
-    print(f"\nfull DiT oracle run: {dt:.1f} s on {oracle.num_threads()} threads = {tflops:.4f} TFLOP/s; "
-          f"worst max-abs error {worst:.3e}")
+    print(f"\nPARITY DiT const max, every row: rows={H * S} max_abs={worst:.3e} mean_abs={err_sum / H:.3e} "
+          f"lse_abs={lse_worst:.3e} oracle_s={dt:.1f} ({oracle.num_threads()} threads, {tflops:.4f} TFLOP/s)",
+          flush=True)
     del q, k, v, o, lse
     torch.cuda.empty_cache()
 
@@ -139,16 +145,26 @@ def test_causal_gqa_full(ca, layout):
 
 def test_dcp_decode_full(ca):
     """64 sequences x 1 token, Hq=32, Hkv=8, D=128, context 131072 over dcp=4
-    shards interleaved in 16-token blocks; sampled sequences checked in full."""
+    shards interleaved in 16-token blocks; every sequence against the oracle
+    (one sequence's shards at a time on the host)."""
     from context_attention_gb300 import synth
 
     N, Hq, Hkv, W, I, Lloc = 64, 32, 8, 4, 16, 32768
     q, k, v = synth.decode_inputs(N, Hq, Hkv, 128, W, Lloc, 5, device="cuda")
     o, lse = ca.dcp_decode(q, k, v, I)
     torch.cuda.synchronize()
-    for n in (0, 37, 63):
-        ro, rl = oracle.dcp_decode(np32(q[n:n + 1]), np32(k[:, n:n + 1]), np32(v[:, n:n + 1]), I)
+    t_oracle = 0.0
+    ros, rls = [], []
+    for n in range(N):
+        qn, kn, vn = np32(q[n:n + 1]), np32(k[:, n:n + 1]), np32(v[:, n:n + 1])
+        t0 = time.perf_counter()
+        ro, rl = oracle.dcp_decode(qn, kn, vn, I)
+        t_oracle += time.perf_counter() - t0
         assert_close(np32(o[n:n + 1]), ro, np32(lse[n:n + 1]), rl, what=f"decode full n={n}")
+        ros.append(ro)
+        rls.append(rl)
+    parity_report("DCP decode 64 seqs L131072 dcp4 (all sequences)", np32(o), np.concatenate(ros), np32(lse),
+                  np.concatenate(rls), t_oracle)
     del q, k, v
     torch.cuda.empty_cache()
 

@@ -5,7 +5,9 @@ import pytest
 import torch
 
 import oracle
-from helpers import assert_close, np32
+import time
+
+from helpers import assert_close, np32, parity_report
 
 pytestmark = pytest.mark.gpu
 
@@ -42,8 +44,11 @@ def test_fp32_tiny_config(ca, mode):
     """fp32, B=1, H=2, S=256, D=64, cp=2: within 1e-4 of the oracle."""
     q, k, v = gen(1, 2, 2, 256, 64, 1, torch.float32)
     o, lse = ca.ring_attn_fwd(q, k, v, 2, mode=mode)
+    t0 = time.perf_counter()
     ro, rl = oracle_ring(q, k, v, 2, mode, False, "contiguous")
+    t = time.perf_counter() - t0
     assert_close(np32(o), ro, np32(lse), rl, dtype=torch.float32, what=f"fp32 {mode}")
+    parity_report(f"tiny fp32 B1 H2 S256 D64 cp2 {mode} (every row)", np32(o), ro, np32(lse), rl, t)
 
 
 @pytest.mark.parametrize("mode", ["online_max", "const_max"])
