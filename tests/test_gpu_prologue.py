@@ -39,11 +39,14 @@ def check_tensor(gpu, ref, what):
 
 
 def run_case(ca, B, S, Hq, Hkv, D, cp, layout, seed, rope=True, gains=True, with_v=True, eps=1e-6):
+    """gains: True (both), False (neither), "q" or "k" (that tensor's only)."""
     x_q, x_k, x_v, g_q, g_k, cos, sin = inputs(B, S, Hq, Hkv, D, seed)
     if not rope:
         cos = sin = None
-    if not gains:
-        g_q = g_k = None
+    if gains is False or gains == "k":
+        g_q = None
+    if gains is False or gains == "q":
+        g_k = None
     q, k, v, km = ca.qkv_prologue(x_q, x_k, Hq, Hkv, x_v=x_v if with_v else None, g_q=g_q, g_k=g_k, eps=eps,
                                   rope_cos=cos, rope_sin=sin, cp_size=cp, layout=layout)
     lay = LAYOUTS[layout]
@@ -84,6 +87,14 @@ def test_prologue_d64_ragged_lanes_no_rope_no_gain_no_v(ca):
     """D = 64, 6 and 3 heads (rows of 48 and 24 chunks: partly filled lanes),
     no rotary tables, no gains, no value tensor, eps = 0."""
     run_case(ca, 2, 96, 6, 3, 64, 3, "striped", seed=23, rope=False, gains=False, with_v=False, eps=0.0)
+
+
+@pytest.mark.parametrize("which", ["q", "k"])
+def test_prologue_one_tensor_with_gains(ca, which):
+    """Only q's or only k's gains given: the block stages just those, and the
+    other tensor is normalised with gain 1 (GQA widths, so the two gain
+    vectors differ in length)."""
+    run_case(ca, 1, 64, 16, 4, 128, 2, "contiguous", seed=25, gains=which)
 
 
 def test_prologue_widest_hidden(ca):
