@@ -85,7 +85,13 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, false, true);
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Online max: the reference moves only when a row's maximum passes it by
+// more than this (log2 units).  P is bf16, which has fp32's exponent range,
+// and a tile's P is kept only when its maximum lies at most 64 above the
+// reference, so P <= 2^64 and O, l stay far from fp32 overflow; a high
+// threshold saves the O rescales that rows with a few very loud keys would
+// otherwise trigger again and again.
+constexpr float kRescaleThreshold = 48.0f;
 constexpr int kMaxRanks = 8;               // segmented schedule
 
 struct TcParams {
@@ -468,8 +474,8 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&r)[32], int ch, int v
 // Online max, speculative single pass over one S row: p = 2^(s*sl2 - m)
 // against the row's current reference m, packed into registers (pk) and
 // summed into sum2, while the row maximum of the raw scores is tracked.
-// Nothing is written to TMEM, so if the maximum turns out to exceed the
-// lazy-rescale threshold the caller still has S to start over from.
+// Nothing is written to TMEM, so if the maximum turns out to lie more than
+// 64 (log2) above the reference the caller still has S to start over from.
 template <bool kMask>
 __device__ __forceinline__ float spec_row(uint32_t tS, int vis_max, uint64_t sl2_2, uint64_t nref_2,
                                           uint32_t (&pk)[64], uint64_t& sum2) {
@@ -893,7 +899,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
             float lo, hi;
             f2_unpack(sum2, lo, hi);
             l += lo + hi;
-            if (jump > kRescaleThreshold) pend = (int)ceilf(jump);  // 9 .. 64
+            if (jump > kRescaleThreshold) pend = (int)ceilf(jump);  // 49 .. 64
             p_done = true;
           }
           mref = m;
