@@ -17,10 +17,11 @@
 // query heads that share a KV head are the N side of warp-level bf16 MMAs
 // (m16n8k16, fp32 accumulate): S^T = K Q^T per 16 tokens, then O^T += V^T P^T,
 // with P moved from the accumulator layout to the operand layout by
-// movmatrix.  Row maxima use the same lazy rescale as the prefill kernel
-// (threshold 2^8).  At the end of an item the four warps' partial states are
-// LSE-merged in shared memory and one partial (o, lse) per query head is
-// written.
+// movmatrix.  Row maxima use a lazy rescale: the reference moves only when a
+// 16-token group's maximum passes it by more than 8 (log2); the rescale of
+// the register-resident O is cheap here.  At the end of an item the four
+// warps' partial states are LSE-merged in shared memory and one partial
+// (o, lse) per query head is written.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
