@@ -353,6 +353,50 @@ size_t ca_dcp_decode_workspace_size(int N, int Hq, int Hkv, int64_t Lloc, int D,
   return align256(sizeof(float) * parts * N * Hq * D) + align256(sizeof(float) * parts * N * Hq);
 }
 
+// The decode entry points share one kernel pair: these fill the arguments
+// they have in common, then place the split-KV partials in the workspace and
+// launch the partial kernel and the LSE merge on the caller's stream.
+static DecodeArgs decode_args(const void* q, const void* k, const void* v, int N, int Hq, int Hkv,
+                              int D, int W, int I, int64_t Lloc, const int32_t* seq_lens,
+                              float softmax_scale) {
+  DecodeArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.N = N;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.W = W;
+  a.I = I;
+  a.Lloc = Lloc;
+  a.seq_lens = seq_lens;
+  a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
+  dcp_decode_split(Lloc, &a.chunk, &a.splits);
+  a.paged = 0;
+  a.block_tables = nullptr;
+  a.nblk = a.max_blocks = 0;
+  a.bs = 0;
+  return a;
+}
+
+static ca_status decode_run(DecodeArgs& a, void* workspace, void* o, float* lse, void* stream) {
+  ca_status st = device_is_gb300();
+  if (st != CA_OK) return st;
+  unsigned* err = device_error_word();
+  if (!err) return CA_ERR_CUDA;
+  const size_t parts = (size_t)a.W * a.splits;
+  a.o_parts = static_cast<float*>(workspace);
+  a.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         align256(sizeof(float) * parts * a.N * a.Hq * a.D));
+  a.err = err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_dcp_decode_partials(a, s);
+  if (e != cudaSuccess) return launched(e);
+  return launched(launch_lse_merge(a.o_parts, a.lse_parts, (int)parts, (int64_t)a.N * a.Hq, a.D, nullptr,
+                                   o, 1, lse, s));
+}
+
 ca_status ca_dcp_decode(const void* q, const void* k_shards, const void* v_shards, ca_dtype dtype,
                         int N, int Hq, int Hkv, int64_t Lloc, int D, int dcp, int interleave,
                         const int32_t* seq_lens, float softmax_scale, void* o, float* lse,
@@ -370,38 +414,9 @@ ca_status ca_dcp_decode(const void* q, const void* k_shards, const void* v_shard
     return CA_ERR_ALIGNMENT;
   const size_t need = ca_dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, dcp, interleave);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return CA_ERR_WORKSPACE;
-  ca_status st = device_is_gb300();
-  if (st != CA_OK) return st;
-  unsigned* err = device_error_word();
-  if (!err) return CA_ERR_CUDA;
-  DecodeArgs a;
-  a.q = q;
-  a.k = k_shards;
-  a.v = v_shards;
-  a.N = N;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.D = D;
-  a.W = dcp;
-  a.I = interleave;
-  a.Lloc = Lloc;
-  a.seq_lens = seq_lens;
-  a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
-  dcp_decode_split(Lloc, &a.chunk, &a.splits);
-  const size_t parts = (size_t)dcp * a.splits;
-  a.o_parts = static_cast<float*>(workspace);
-  a.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                         align256(sizeof(float) * parts * N * Hq * D));
-  a.err = err;
-  a.paged = 0;
-  a.block_tables = nullptr;
-  a.nblk = a.max_blocks = 0;
-  a.bs = 0;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_dcp_decode_partials(a, s);
-  if (e != cudaSuccess) return launched(e);
-  return launched(launch_lse_merge(a.o_parts, a.lse_parts, (int)parts, (int64_t)N * Hq, D, nullptr,
-                                   o, 1, lse, s));
+  DecodeArgs a = decode_args(q, k_shards, v_shards, N, Hq, Hkv, D, dcp, interleave, Lloc, seq_lens,
+                             softmax_scale);
+  return decode_run(a, workspace, o, lse, stream);
 }
 
 size_t ca_ring_decode_workspace_size(int B, int Hq, int Hkv, int64_t S, int D, int cp_size) {
@@ -431,41 +446,11 @@ ca_status ca_ring_decode(const void* q, const void* k, const void* v, ca_dtype d
     return CA_ERR_ALIGNMENT;
   const size_t need = ca_ring_decode_workspace_size(B, Hq, Hkv, S, D, cp_size);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return CA_ERR_WORKSPACE;
-  ca_status st = device_is_gb300();
-  if (st != CA_OK) return st;
-  unsigned* err = device_error_word();
-  if (!err) return CA_ERR_CUDA;
   // the decode kernel over the ring layout: sequence n = batch element b,
   // W = cp shards of Lloc = S/cp rows each
-  DecodeArgs a;
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.N = B;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.D = D;
-  a.W = cp_size;
-  a.I = 1;
-  a.Lloc = S / cp_size;
-  a.seq_lens = seq_lens;
-  a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
-  dcp_decode_split(a.Lloc, &a.chunk, &a.splits);
-  const size_t parts = (size_t)cp_size * a.splits;
-  a.o_parts = static_cast<float*>(workspace);
-  a.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                         align256(sizeof(float) * parts * B * Hq * D));
-  a.err = err;
-  a.paged = 0;
-  a.block_tables = nullptr;
-  a.nblk = a.max_blocks = 0;
-  a.bs = 0;
+  DecodeArgs a = decode_args(q, k, v, B, Hq, Hkv, D, cp_size, 1, S / cp_size, seq_lens, softmax_scale);
   a.ring_layout = (int)layout;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_dcp_decode_partials(a, s);
-  if (e != cudaSuccess) return launched(e);
-  return launched(launch_lse_merge(a.o_parts, a.lse_parts, (int)parts, (int64_t)B * Hq, D, nullptr,
-                                   o, 1, lse, s));
+  return decode_run(a, workspace, o, lse, stream);
 }
 
 ca_status ca_dcp_decode_paged(const void* q, const void* k_cache, const void* v_cache,
@@ -490,39 +475,14 @@ ca_status ca_dcp_decode_paged(const void* q, const void* k_cache, const void* v_
   const int64_t Lloc = max_blocks * block_size;
   const size_t need = ca_dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, dcp, interleave);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return CA_ERR_WORKSPACE;
-  ca_status st = device_is_gb300();
-  if (st != CA_OK) return st;
-  unsigned* err = device_error_word();
-  if (!err) return CA_ERR_CUDA;
-  DecodeArgs a;
-  a.q = q;
-  a.k = k_cache;
-  a.v = v_cache;
-  a.N = N;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.D = D;
-  a.W = dcp;
-  a.I = interleave;
-  a.Lloc = Lloc;
-  a.seq_lens = seq_lens;
-  a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
-  dcp_decode_split(Lloc, &a.chunk, &a.splits);
-  const size_t parts = (size_t)dcp * a.splits;
-  a.o_parts = static_cast<float*>(workspace);
-  a.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                         align256(sizeof(float) * parts * N * Hq * D));
-  a.err = err;
+  DecodeArgs a = decode_args(q, k_cache, v_cache, N, Hq, Hkv, D, dcp, interleave, Lloc, seq_lens,
+                             softmax_scale);
   a.paged = 1;
   a.block_tables = block_tables;
   a.nblk = nblk;
   a.max_blocks = max_blocks;
   a.bs = block_size;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_dcp_decode_partials(a, s);
-  if (e != cudaSuccess) return launched(e);
-  return launched(launch_lse_merge(a.o_parts, a.lse_parts, (int)parts, (int64_t)N * Hq, D, nullptr,
-                                   o, 1, lse, s));
+  return decode_run(a, workspace, o, lse, stream);
 }
 
 ca_status ca_paged_kv_write(const void* k_new, const void* v_new, const int64_t* slots,
