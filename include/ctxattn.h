@@ -29,6 +29,9 @@
  *   (CA_LAYOUT_STRIPED, [SHI]: token t on shard t mod cp).  Outputs use the
  *   same row order as q.
  * - Causal: key j is visible to query i iff global(j) <= global(i).
+ * - Sizes (batch, heads, rows, head dimension, sequences, shards) must be
+ *   positive: an empty problem is CA_ERR_INVALID_ARG.  The one exception is
+ *   ca_paged_kv_write with T = 0 new tokens, a valid no-op.
  * - Errors: every call validates its arguments on the host first and returns
  *   a ca_status; on a host-side error nothing is enqueued and nothing is
  *   written.  There is no fallback path: an unsupported case is an error.

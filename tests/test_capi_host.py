@@ -217,3 +217,21 @@ def test_qkv_prologue_validation(ca):
     assert S[pro(S=1 << 30, cp=1)] == "CA_ERR_UNSUPPORTED"  # rows past 32-bit indices
     assert S[pro(k=FAKE + 8)] == "CA_ERR_ALIGNMENT"
     assert S[pro(km=FAKE + 2)] == "CA_ERR_ALIGNMENT"
+
+
+def test_empty_problems(ca):
+    """A problem with no rows, heads or sequences is an invalid argument
+    (nothing is enqueued); the one exception is the paged cache write, for
+    which zero new tokens is a valid no-op that touches no device."""
+    lib = ca._load()
+    S = ca.STATUS
+    for kw in (dict(S=0), dict(B=0), dict(Hq=0), dict(Hkv=0), dict(D=0)):
+        assert S[ring(lib, **kw)] == "CA_ERR_INVALID_ARG", kw
+    assert S[lib.ca_dcp_decode(FAKE, FAKE, FAKE, 1, 0, 8, 2, 256, 128, 4, 16, None, 0.0, FAKE, None, FAKE,
+                               1 << 30, None)] == "CA_ERR_INVALID_ARG"
+    assert S[lib.ca_ring_decode(FAKE, FAKE, FAKE, 1, 0, 8, 2, 1024, 128, 4, 0, None, 0.0, FAKE, None, FAKE,
+                                1 << 30, None)] == "CA_ERR_INVALID_ARG"
+    assert S[lib.ca_qkv_prologue(FAKE, FAKE, None, None, None, 1e-6, None, None, 1, 1, 0, 8, 2, 128, 4, 0,
+                                 FAKE, FAKE, None, None, None)] == "CA_ERR_INVALID_ARG"
+    assert S[lib.ca_key_max2(FAKE, 1, 1, 2, 0, 128, FAKE, None)] == "CA_ERR_INVALID_ARG"
+    assert S[lib.ca_paged_kv_write(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 0, 2, 128, 4, 64, 16, None)] == "CA_OK"
