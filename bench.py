@@ -159,6 +159,24 @@ def barrier(pg):
         pg.barrier()
 
 
+# a timed region whose clocks saw one of these is not a valid measurement:
+# it is taken once more (sw_power_cap is normal under load and is kept)
+REJECTED_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def timed_with_retry(timed, pg):
+    """Run the timed region; if any rank's clocks saw a rejected slowdown,
+    run it once more (all ranks together) and keep the second result, noting
+    the first run's reasons in its clock summary."""
+    res = timed()
+    bad = any(r in REJECTED_REASONS for r in res["clocks"].get("reasons", []))
+    if max_over_ranks(float(bad), pg) > 0:
+        first = res["clocks"].get("reasons", [])
+        res = timed()
+        res["clocks"]["remeasured_after"] = first
+    return res
+
+
 def max_over_ranks(x, pg):
     """Max of a float over all ranks (the job's time is its slowest rank's)."""
     if pg is None:
@@ -209,26 +227,27 @@ def bench_prefill(ca, torch, steps, warmup, pg, dev_index):
     torch.cuda.synchronize()
     barrier(pg)
     torch.cuda.synchronize()
-    evs = []
-    with ClockSampler(dev_index) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        prev = t_start
-        for _ in range(steps):
-            mid = step()
-            end = torch.cuda.Event(enable_timing=True)
-            end.record(stream)
-            evs.append((prev, mid, end))
-            prev = end
+    def timed():
+        evs = []
+        with ClockSampler(dev_index) as clk:
+            t_start = torch.cuda.Event(enable_timing=True)
+            t_start.record(stream)
+            prev = t_start
+            for _ in range(steps):
+                mid = step()
+                end = torch.cuda.Event(enable_timing=True)
+                end.record(stream)
+                evs.append((prev, mid, end))
+                prev = end
+            torch.cuda.synchronize()
+        barrier(pg)
         torch.cuda.synchronize()
-    barrier(pg)
-    torch.cuda.synchronize()
-    total_ms = t_start.elapsed_time(prev)
-    ring_ms = [m.elapsed_time(e) for _, m, e in evs]
-    bound_ms = [s.elapsed_time(m) for s, m, _ in evs]
+        return dict(total_ms=t_start.elapsed_time(prev),
+                    ring_ms=statistics.mean([m.elapsed_time(e) for _, m, e in evs]),
+                    bound_ms=statistics.mean([s.elapsed_time(m) for s, m, _ in evs]), clocks=clk.summary())
+
+    res = timed_with_retry(timed, pg)
     assert ca.device_status() == 0
-    res = dict(total_ms=total_ms, ring_ms=statistics.mean(ring_ms), bound_ms=statistics.mean(bound_ms),
-               clocks=clk.summary())
     # e2e: through the public API from pinned host memory.  Every step copies
     # its q, k, v host->device and its o device->host inside the timed region;
     # the copies of one step overlap the attention of the previous one (two
@@ -316,20 +335,23 @@ def bench_decode(ca, torch, steps, warmup, pg, dev_index):
     torch.cuda.synchronize()
     barrier(pg)
     torch.cuda.synchronize()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(dev_index) as clk:
-        a.record(stream)
-        for _ in range(steps):
-            ca.dcp_decode(q, k, v, c["I"], out=o, lse=lse, workspace=ws)
-        b.record(stream)
-        torch.cuda.synchronize()
-    barrier(pg)
-    ms = a.elapsed_time(b) / steps
+    def timed():
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(dev_index) as clk:
+            a.record(stream)
+            for _ in range(steps):
+                ca.dcp_decode(q, k, v, c["I"], out=o, lse=lse, workspace=ws)
+            b.record(stream)
+            torch.cuda.synchronize()
+        barrier(pg)
+        return dict(ms=a.elapsed_time(b) / steps, clocks=clk.summary())
+
+    res = timed_with_retry(timed, pg)
     assert ca.device_status() == 0
     del q, k, v
     torch.cuda.empty_cache()
-    return dict(ms=ms, clocks=clk.summary())
+    return res
 
 
 class OracleSampler:

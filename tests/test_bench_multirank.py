@@ -56,3 +56,25 @@ def test_single_rank_needs_no_process_group():
 
     assert bench.max_over_ranks(3.5, None) == 3.5
     assert bench.aggregate_throughput(1e12, 10, 1, 1000.0) == pytest.approx(1e13)
+
+
+def test_rejected_clocks_are_measured_once_more():
+    """A timed region whose clocks saw a thermal or hardware slowdown is run
+    once more and the second result kept, with the first run's reasons noted;
+    power capping alone is kept as it is."""
+    import bench
+
+    runs = []
+
+    def timed(reasons_by_run):
+        def f():
+            runs.append(1)
+            return {"ms": float(len(runs)), "clocks": {"reasons": list(reasons_by_run[len(runs) - 1])}}
+        return f
+
+    r = bench.timed_with_retry(timed([["hw_thermal_slowdown", "sw_power_cap"], ["sw_power_cap"]]), None)
+    assert len(runs) == 2 and r["ms"] == 2.0
+    assert r["clocks"]["remeasured_after"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    runs.clear()
+    r = bench.timed_with_retry(timed([["sw_power_cap"]]), None)
+    assert len(runs) == 1 and "remeasured_after" not in r["clocks"]
