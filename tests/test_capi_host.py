@@ -64,6 +64,9 @@ def test_ring_validation_codes(ca):
     assert S[ring(lib, D=64)] == "CA_ERR_UNSUPPORTED"           # bf16 needs D = 128
     assert S[ring(lib, dtype=0, D=160)] == "CA_ERR_UNSUPPORTED"  # fp32 needs D <= 128
     assert S[ring(lib, q=FAKE + 2)] == "CA_ERR_ALIGNMENT"
+    # the kernels view q as a [B*Hq*S, D] matrix with 32-bit row indices
+    assert S[ring(lib, B=1 << 12, Hq=8, Hkv=8, S=1 << 16, cp=8)] == "CA_ERR_UNSUPPORTED"
+    assert S[ring(lib, B=1 << 12, Hq=8, Hkv=8, S=(1 << 16) - 8, cp=8, q=None)] == "CA_ERR_INVALID_ARG"
     assert S[ring(lib, mode=1)] == "CA_ERR_WORKSPACE"            # const max needs the bound buffer
     need = lib.ca_ring_attn_fwd_workspace_size(1, 4, 2, 1024, 128, 4, 1)
     assert need >= 4 * 2                                         # kmax2 [B, Hkv]
@@ -135,6 +138,7 @@ def test_merge_bound_decode_layout_validation(ca):
     assert S[dec(Hq=6, Hkv=4)] == "CA_ERR_SHAPE"
     assert S[dec(dtype=0)] == "CA_ERR_UNSUPPORTED"
     assert S[dec(Hq=32, Hkv=2)] == "CA_ERR_UNSUPPORTED"  # more than 8 query heads per KV head
+    assert S[dec(N=1 << 14, Hkv=8, Hq=8, Lloc=1 << 16, W=2)] == "CA_ERR_UNSUPPORTED"  # 2^31 cache rows
     assert S[dec(ws=None)] == "CA_ERR_WORKSPACE"
     assert S[dec(ws_bytes=16)] == "CA_ERR_WORKSPACE"
     assert lib.ca_dcp_decode_workspace_size(64, 32, 8, 32768, 128, 4, 16) > 64 * 32 * 128 * 4 * 4
