@@ -3,6 +3,7 @@
 // point validates on the host before it touches the device; on a host-side
 // error nothing is enqueued.  There is no CPU or fallback path: a case no
 // kernel supports returns CA_ERR_UNSUPPORTED.
+#include <atomic>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -15,12 +16,16 @@
 
 namespace ca {
 
+// The per-device caches below (and the kernels' shared-memory attribute
+// flags) may be filled by concurrent first calls from several host threads:
+// they are atomic, and every writer stores the same value.
+
 // Device error word raised by bounded waits (see ptx.cuh).  Kernels get its
 // device address from device_error_word().
 static __device__ unsigned g_error_word;
 
 static unsigned* device_error_word() {
-  static unsigned* cache[64] = {nullptr};
+  static std::atomic<unsigned*> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   if (!cache[dev]) {
@@ -32,7 +37,7 @@ static unsigned* device_error_word() {
 }
 
 int device_sm_count() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
   if (!cache[dev]) {
@@ -44,7 +49,7 @@ int device_sm_count() {
 }
 
 static bool trace_enabled() {
-  static int t = -1;
+  static std::atomic<int> t{-1};
   if (t < 0) {
     const char* e = getenv("CTXATTN_TRACE");
     t = (e && e[0] && e[0] != '0') ? 1 : 0;

@@ -22,6 +22,7 @@
 // the register-resident O is cheap here.  At the end of an item the four
 // warps' partial states are LSE-merged in shared memory and one partial
 // (o, lse) per query head is written.
+#include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -424,7 +425,7 @@ void dcp_decode_split(int64_t Lloc, int64_t* chunk, int* splits) {
 template <bool kPaged>
 static cudaError_t launch_decode(const DecParams& P, const CUtensorMap& tk, const CUtensorMap& tv,
                                  cudaStream_t stream) {
-  static int attr_set[64] = {0};
+  static std::atomic<int> attr_set[64];  // idempotent once-per-device setup
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {

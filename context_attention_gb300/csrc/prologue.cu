@@ -25,6 +25,7 @@
 // reads), kept as a per-warp running max in shared memory and merged into
 // kmax2[b, h] with one atomicMax per head whenever the warp's tokens move
 // to another batch element.
+#include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -371,7 +372,7 @@ cudaError_t launch_qkv_prologue(const QkvPrologueArgs& q, cudaStream_t stream) {
   const int64_t nwarps = (ntok + a.jobs_per_warp - 1) / a.jobs_per_warp;
   const unsigned blocks = (unsigned)((nwarps + warps - 1) / warps);
   auto kern = q.D == 128 ? prologue_kernel<128> : prologue_kernel<64>;
-  static int attr_set[64][2] = {{0}};
+  static std::atomic<int> attr_set[64][2];  // idempotent once-per-device setup
   int dev = 0;
   cudaGetDevice(&dev);
   const int di = q.D == 128;

@@ -29,6 +29,7 @@
 // the new tile maximum exceeds it by more than 8 (log2 units), so P stays
 // <= 256 and O is rescaled in TMEM only on those rare tiles.  Const max never
 // rescales: merging the ring steps is pure addition.
+#include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -1025,7 +1026,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
 
 template <bool kConst>
 static cudaError_t launch_tc_mode(const TcMaps& maps, const TcParams& P, cudaStream_t stream) {
-  static int attr_set[64] = {0};
+  static std::atomic<int> attr_set[64];  // idempotent once-per-device setup
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
