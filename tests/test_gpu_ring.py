@@ -320,3 +320,44 @@ def test_striped_ring_equals_contiguous_after_unpermuting(ca):
     d = (back.float() - oc.float()).abs()
     assert d.max().item() <= 2e-2 and d.mean().item() <= 2e-3
     assert (lback - lc).abs().max().item() <= 1e-3
+
+
+def test_concurrent_calls_from_two_threads(ca):
+    """Two host threads, each with its own stream, call the library at the
+    same time (the ring on one, DCP decode on the other, repeatedly); every
+    result is bit-identical to the same call made alone."""
+    import threading
+
+    from context_attention_gb300 import synth
+
+    q, k, v = gen(1, 4, 2, 1024, 128, 51, torch.bfloat16)
+    qd, kd, vd = synth.decode_inputs(4, 8, 2, 128, 4, 512, 52, device="cuda")
+    o_ref, l_ref = ca.ring_attn_fwd(q, k, v, 4, mode="online_max", causal=True, layout="striped")
+    od_ref, ld_ref = ca.dcp_decode(qd, kd, vd, 16)
+    torch.cuda.synchronize()
+    results, errors = {}, []
+
+    def worker(name, fn):
+        try:
+            s = torch.cuda.Stream()
+            outs = []
+            with torch.cuda.stream(s):
+                for _ in range(8):
+                    outs.append(fn())
+            s.synchronize()
+            results[name] = outs
+        except Exception as e:  # noqa: BLE001 -- reported below
+            errors.append(e)
+
+    t1 = threading.Thread(target=worker, args=("ring", lambda: ca.ring_attn_fwd(q, k, v, 4, mode="online_max",
+                                                                                 causal=True, layout="striped")))
+    t2 = threading.Thread(target=worker, args=("decode", lambda: ca.dcp_decode(qd, kd, vd, 16)))
+    t1.start()
+    t2.start()
+    t1.join()
+    t2.join()
+    assert not errors, errors
+    for o, lse in results["ring"]:
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+    for o, lse in results["decode"]:
+        assert torch.equal(o, od_ref) and torch.equal(lse, ld_ref)
