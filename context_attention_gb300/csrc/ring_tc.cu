@@ -19,16 +19,19 @@
 //                    the end normalises O and writes o and lse;
 //   warp 8           TMA producer: Q tiles, then K and V tiles of every ring
 //                    step in order, through a 5-slot ring of 32 KB buffers;
-//   warp 9           tcgen05 issuer (one thread): S_i = Q_i K^T and
-//                    O_i += P_i V for both tiles, interleaved so that one
-//                    tile's softmax overlaps the other tile's matrix products.
+//   warp 9           tcgen05 issuer: the whole warp walks the schedule (its
+//                    descriptors stay warp-uniform) and lane 0 issues
+//                    S_i = Q_i K^T and O_i += P_i V for both tiles,
+//                    interleaved so that one tile's softmax overlaps the other
+//                    tile's matrix products.
 // TMEM (512 columns): S0, S1 (fp32, 128 each; P aliases their first 64), O0,
 // O1 (fp32, 128 each).  The accumulators never leave TMEM until the unit ends.
 //
 // Online max uses a lazy rescale: a row's reference maximum only moves when
-// the new tile maximum exceeds it by more than 8 (log2 units), so P stays
-// <= 256 and O is rescaled in TMEM only on those rare tiles.  Const max never
-// rescales: merging the ring steps is pure addition.
+// a tile's maximum exceeds it by more than kRescaleThreshold (log2 units), so
+// O is rescaled in TMEM only on those rare tiles; bf16 P keeps fp32's range,
+// so P may grow far above 1 meanwhile.  Const max never rescales: merging the
+// ring steps is pure addition.
 #include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
