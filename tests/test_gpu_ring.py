@@ -361,3 +361,33 @@ def test_concurrent_calls_from_two_threads(ca):
         assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
     for o, lse in results["decode"]:
         assert torch.equal(o, od_ref) and torch.equal(lse, ld_ref)
+
+
+def test_calls_replay_inside_a_cuda_graph(ca):
+    """The entry points only enqueue work on the caller's stream, so a caller
+    can capture them in a CUDA graph (after one warm-up call per kernel, which
+    sets the kernels' shared-memory limits): replaying the graph on new
+    inputs gives the same bits as eager calls."""
+    from context_attention_gb300 import synth
+
+    q, k, v = gen(1, 4, 4, 2048, 128, 61, torch.bfloat16)
+    qd, kd, vd = synth.decode_inputs(4, 8, 2, 128, 4, 512, 62, device="cuda")
+    ca.ring_attn_fwd(q, k, v, 4, mode="const_max")
+    ca.dcp_decode(qd, kd, vd, 16)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        o, lse = ca.ring_attn_fwd(q, k, v, 4, mode="const_max")
+        od, ld = ca.dcp_decode(qd, kd, vd, 16)
+    for seed in (63, 64):
+        q2, k2, v2 = gen(1, 4, 4, 2048, 128, seed, torch.bfloat16)
+        q.copy_(q2), k.copy_(k2), v.copy_(v2)
+        qd.copy_(torch.randn_like(qd.float()).to(qd.dtype))
+        g.replay()
+        torch.cuda.synchronize()
+        o_e, l_e = ca.ring_attn_fwd(q, k, v, 4, mode="const_max")
+        od_e, ld_e = ca.dcp_decode(qd, kd, vd, 16)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_e) and torch.equal(lse, l_e)
+        assert torch.equal(od, od_e) and torch.equal(ld, ld_e)
+    assert ca.device_status() == 0
