@@ -61,6 +61,17 @@ def test_fp32_gqa_ragged_causal(ca, mode, causal, layout):
     assert_close(np32(o), ro, np32(lse), rl, dtype=torch.float32, what=f"fp32 {mode} {layout}")
 
 
+@pytest.mark.parametrize("mode", ["online_max", "const_max"])
+@pytest.mark.parametrize("D", [1, 17, 100])
+def test_fp32_odd_head_dims(ca, mode, D):
+    """fp32 with head dimensions whose rows are not whole 16-byte chunks (the
+    key pass's scalar path), causal striped, GQA 4:2."""
+    q, k, v = gen(1, 4, 2, 192, D, 3 + D, torch.float32)
+    o, lse = ca.ring_attn_fwd(q, k, v, 2, mode=mode, causal=True, layout="striped")
+    ro, rl = oracle_ring(q, k, v, 2, mode, True, "striped")
+    assert_close(np32(o), ro, np32(lse), rl, dtype=torch.float32, what=f"fp32 D={D} {mode}")
+
+
 # --------------------------------------------------------------- bf16 (tcgen05)
 
 
@@ -202,7 +213,8 @@ def test_key_max2_kernel(ca):
     from context_attention_gb300 import synth
 
     for dtype, D, S in ((torch.bfloat16, 128, 700), (torch.float32, 128, 333), (torch.bfloat16, 48, 257),
-                        (torch.float32, 20, 700), (torch.bfloat16, 128, 1)):
+                        (torch.float32, 20, 700), (torch.bfloat16, 128, 1), (torch.float32, 17, 300),
+                        (torch.float32, 1, 50)):
         _, k, _ = synth.normal_qkv(2, 2, 3, S, D, 12, dtype=dtype, device="cuda")
         km = ca.key_max2(k)
         _, rk = oracle.const_max_bound(np32(k), np32(k))
