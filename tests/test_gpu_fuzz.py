@@ -2,7 +2,8 @@
 -- ring attention (ragged shard lengths, GQA ratios, shard counts 1-8, both
 layouts, both modes, causal or not, fp32 head dimensions 1-128), DCP and ring
 decode (random shard counts, interleaves and sequence lengths, empty ones
-included), the QKV prologue (random head counts, widths and options) -- so
+included), DCP prefill and paged decode, the QKV prologue (random head
+counts, widths and options) -- so
 shape combinations no hand-written case names are still compared element by
 element."""
 import numpy as np
@@ -160,3 +161,47 @@ def test_qkv_prologue_random_shapes(ca, c):
                                                                              cp=c["cp"], layout=lay)), str(c)
     _, rkm = oracle.const_max_bound(np32(k), np32(k))
     np.testing.assert_allclose(np32(km), rkm, rtol=2e-6, err_msg=str(c))
+
+
+def prefill_draws(n, seed):
+    rng = np.random.default_rng(seed)
+    for i in range(n):
+        yield dict(i=i, Hkv=int(rng.integers(1, 4)), G=int(rng.integers(1, 5)), W=int(rng.choice([1, 2, 4, 8])),
+                   I=int(rng.choice([16, 32])), Sc=int(rng.integers(1, 700)), P=int(rng.integers(0, 3000)),
+                   seed=int(rng.integers(0, 1 << 30)))
+
+
+@pytest.mark.parametrize("c", list(prefill_draws(16, 2030)), ids=lambda c: f"draw{c['i']}")
+def test_dcp_prefill_random_shapes(ca, c):
+    from test_gpu_dcp_prefill import clean, make
+
+    q, kp, vp, kc, vc = make(ca, c["Hkv"] * c["G"], c["Hkv"], c["W"], c["I"], c["Sc"], c["P"], seed=c["seed"])
+    o, lse = ca.dcp_prefill(q, kp, vp, kc, vc, c["I"], c["P"])
+    ro, rl = oracle.dcp_prefill(np32(q), clean(kp), clean(vp), clean(kc), clean(vc), c["I"], c["P"])
+    assert_close(np32(o), ro, np32(lse), rl, what=str(c))
+
+
+def paged_draws(n, seed):
+    rng = np.random.default_rng(seed)
+    for i in range(n):
+        bs = int(rng.choice([8, 16, 32, 64, 128]))
+        yield dict(i=i, N=int(rng.integers(1, 4)), Hkv=int(rng.integers(1, 3)), G=int(rng.integers(1, 9)),
+                   W=int(rng.integers(1, 5)), bs=bs, mb=int(rng.integers(1, 12)), seed=int(rng.integers(0, 1 << 30)))
+
+
+@pytest.mark.parametrize("c", list(paged_draws(16, 2031)), ids=lambda c: f"draw{c['i']}")
+def test_paged_decode_random_shapes(ca, c):
+    from context_attention_gb300 import synth
+    from test_gpu_paged_decode import page
+
+    Lloc = c["bs"] * c["mb"]
+    q, ks, vs = synth.decode_inputs(c["N"], c["Hkv"] * c["G"], c["Hkv"], 128, c["W"], Lloc, c["seed"], device="cuda")
+    rng = np.random.default_rng(c["seed"])
+    lens = [int(x) for x in rng.integers(0, c["W"] * Lloc + 1, size=c["N"])]
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    kc, vc, bt = page(ks, vs, c["bs"], seed=c["seed"] % 1000)
+    o, lse = ca.dcp_decode_paged(q, kc, vc, bt, c["bs"], sl)
+    o_c, l_c = ca.dcp_decode(q, ks, vs, c["bs"], seq_lens=sl)
+    assert torch.equal(o, o_c) and torch.equal(lse, l_c), str(c)
+    ro, rl = oracle.dcp_decode(np32(q), np32(ks), np32(vs), c["bs"], seq_lens=lens)
+    assert_close(np32(o), ro, np32(lse), rl, what=f"{c} lens={lens}")
