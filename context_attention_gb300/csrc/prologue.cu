@@ -37,7 +37,7 @@
 namespace ca {
 namespace {
 
-constexpr int kMaxWarps = 16;     // per block (one block per SM)
+constexpr int kMaxWarps = 18;     // per block (one block per SM)
 constexpr int kMaxHeads = 128;    // H * D <= 8192 and D >= 64
 constexpr int kMaxBufs = 4;       // row buffers per warp
 
@@ -352,11 +352,13 @@ cudaError_t launch_qkv_prologue(const QkvPrologueArgs& q, cudaStream_t stream) {
   const int64_t ntok = (int64_t)q.B * q.S;
   if (ntok == 0) return cudaSuccess;
   a.err = q.err;
-  // one block per SM; buffers sized for the longest row, as many warps as
-  // shared memory holds.  Long rows get one buffer per warp (the next row is
-  // requested as soon as the current one has been read): more warps, each
-  // with one row in flight, outrun fewer warps that prefetch deeper.  Short
-  // rows get more buffers, so that a warp keeps about 8 KB or more in flight.
+  // one block per SM; buffers sized for the longest row.  Long rows get one
+  // buffer per warp (the next row is requested as soon as the current one has
+  // been read): more warps, each with one row in flight, outrun fewer warps
+  // that prefetch deeper.  Short rows get more buffers, so that a warp keeps
+  // about 8 KB or more in flight.  Warps: as many as shared memory holds, up
+  // to ~160 KB of rows in flight per SM (measured: beyond that the extra
+  // copies only queue in the memory system and the kernel slows down).
   const uint32_t row_bytes = (uint32_t)max_h * q.D * 2;
   a.buf_bytes = (row_bytes + 127) / 128 * 128;
   a.nbuf = a.buf_bytes >= 8192 ? 1 : a.buf_bytes >= 4096 ? 2 : kMaxBufs;
@@ -364,6 +366,7 @@ cudaError_t launch_qkv_prologue(const QkvPrologueArgs& q, cudaStream_t stream) {
   a.gain_floats = (uint32_t)((q.g_q ? q.Hq : 0) + (q.g_k ? q.Hkv : 0)) * q.D;
   const uint32_t gain_bytes = (a.gain_floats * 4 + 127) / 128 * 128;
   int warps = kMaxWarps;
+  while (warps > 1 && (uint32_t)warps * a.nbuf * a.buf_bytes > 160u * 1024u) --warps;
   while (warps > 1 && pro_head_bytes(warps) + gain_bytes + (uint32_t)warps * a.nbuf * a.buf_bytes > kSmemBudget)
     --warps;
   const uint32_t smem = pro_head_bytes(warps) + gain_bytes + (uint32_t)warps * a.nbuf * a.buf_bytes;
