@@ -50,6 +50,7 @@ class CtxAttnError(RuntimeError):
 
 
 def library_path() -> str:
+    """Path of the in-tree libctxattn.so the binding loads."""
     return _LIB_PATH
 
 
@@ -135,6 +136,7 @@ def _need(t: torch.Tensor, name: str, ndim: int):
 
 
 def ring_attn_fwd_workspace_size(B, Hq, Hkv, S, D, cp_size, mode="online_max") -> int:
+    """Workspace bytes ring_attn_fwd needs (const max: the key maximum kmax2; online max: 0)."""
     return int(_load().ca_ring_attn_fwd_workspace_size(B, Hq, Hkv, S, D, cp_size, MODE[mode]))
 
 
@@ -303,6 +305,7 @@ def ring_decode_workspace_size(B, Hq, Hkv, S, D, cp_size):
 
 
 def dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, dcp, interleave) -> int:
+    """Workspace bytes of dcp_decode / dcp_decode_paged (its split-KV partials)."""
     return int(_load().ca_dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, dcp, interleave))
 
 
@@ -510,34 +513,42 @@ def dcp_shard_kv(kv, dcp, interleave):
 
 # ------------------------------------------------------------- host index helpers
 def layout_global_index(layout, cp_size, Ls, row) -> int:
+    """Global token position of stored row r*Ls + a (contiguous: r*Ls + a; striped: a*cp + r)."""
     return int(_load().ca_layout_global_index(LAYOUT[layout], cp_size, Ls, row))
 
 
 def layout_shard_row(layout, cp_size, Ls, token) -> int:
+    """Stored row of a global token: the inverse of layout_global_index."""
     return int(_load().ca_layout_shard_row(LAYOUT[layout], cp_size, Ls, token))
 
 
 def ring_kv_shard(rank, step, cp_size) -> int:
+    """K/V shard that shard `rank` meets at ring step `step`: (rank - step) mod cp_size."""
     return int(_load().ca_ring_kv_shard(rank, step, cp_size))
 
 
 def dcp_owner(pos, dcp, interleave) -> int:
+    """DCP rank holding global position pos: (pos // interleave) mod dcp."""
     return int(_load().ca_dcp_owner(pos, dcp, interleave))
 
 
 def dcp_local_index(pos, dcp, interleave) -> int:
+    """Local slot of pos on its owner rank: (pos // (dcp*I))*I + pos % I."""
     return int(_load().ca_dcp_local_index(pos, dcp, interleave))
 
 
 def dcp_local_to_global(local, rank, dcp, interleave) -> int:
+    """Global position of local slot s on a rank: (s // I)*(dcp*I) + rank*I + s % I."""
     return int(_load().ca_dcp_local_to_global(local, rank, dcp, interleave))
 
 
 def dcp_local_filled(N, dcp, interleave, block_size, rank) -> int:
+    """Tokens among positions [0, N) a rank holds (the DCP page's local_filled formula)."""
     return int(_load().ca_dcp_local_filled(N, dcp, interleave, block_size, rank))
 
 
 def dcp_active_mask(N, dcp, interleave, block_size, rank) -> int:
+    """1 if `rank` owns the token at position N (the decoded token), else 0."""
     return int(_load().ca_dcp_active_mask(N, dcp, interleave, block_size, rank))
 
 
