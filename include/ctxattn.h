@@ -105,7 +105,8 @@ int ca_version(void);
  *             quantities inside a pass already paid for).
  * Errors: CA_ERR_SHAPE if S % cp_size != 0 ([CP] "Sequence Length
  * Constraints": S=3645 with cp_size=8 is rejected) or Hq % Hkv != 0;
- * CA_ERR_UNSUPPORTED for bf16 with D != 128.
+ * CA_ERR_UNSUPPORTED for bf16 with D != 128 or B*Hq*S >= 2^31 (the kernel
+ * addresses rows with 32-bit indices), and for fp32 with D > 128.
  * ---------------------------------------------------------------------- */
 size_t ca_ring_attn_fwd_workspace_size(int B, int Hq, int Hkv, int64_t S, int D,
                                        int cp_size, ca_mode mode);
