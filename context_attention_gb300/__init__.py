@@ -25,7 +25,8 @@ __all__ = [
     "layout_to_shards", "layout_from_shards", "dcp_shard_kv",
     "layout_global_index", "layout_shard_row", "ring_kv_shard", "dcp_owner", "dcp_local_index",
     "dcp_local_to_global", "dcp_local_filled", "dcp_active_mask", "dcp_slot_mapping",
-    "device_status", "ring_attn_fwd_workspace_size", "dcp_decode_workspace_size", "ring_decode_workspace_size",
+    "device_status", "selftest_wait_timeout",
+    "ring_attn_fwd_workspace_size", "dcp_decode_workspace_size", "ring_decode_workspace_size",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -104,6 +105,7 @@ def _load():
             "ca_dcp_active_mask": ([I64, I, I, I, I], I),
             "ca_dcp_slot_mapping": ([P, I64, P, I64, I, I, I, I, P], I),
             "ca_device_status": ([I], I),
+            "ca_selftest_wait_timeout": ([ctypes.c_longlong, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -563,6 +565,15 @@ def dcp_slot_mapping(positions, block_table, block_size, dcp, rank, interleave):
                                       dcp, rank, interleave, out.ctypes.data)
     _check("ca_dcp_slot_mapping", st)
     return out
+
+
+def selftest_wait_timeout(limit_cycles: int = 2_000_000):
+    """Run the failure-path diagnostic on the current stream: one warp's
+    bounded wait on a barrier nothing completes gives up after
+    `limit_cycles` cycles and raises the device error word (read it with
+    device_status())."""
+    _check("ca_selftest_wait_timeout", _load().ca_selftest_wait_timeout(int(limit_cycles),
+                                                                        torch.cuda.current_stream().cuda_stream))
 
 
 def device_status(reset: bool = True) -> int:

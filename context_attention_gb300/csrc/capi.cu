@@ -13,6 +13,7 @@
 #include "../../include/ctxattn.h"
 #include "index_maps.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace ca {
 
@@ -34,6 +35,21 @@ static unsigned* device_error_word() {
     cache[dev] = static_cast<unsigned*>(p);
   }
   return cache[dev];
+}
+
+// Diagnostic: one warp waits on an mbarrier that nothing ever completes.
+// The bounded wait gives up after `limit` cycles and raises the device
+// error word, exactly as a stalled pipeline's waits would, without a fault.
+__global__ void wait_timeout_kernel(unsigned* err, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_cycles(smem_u32(&bar), 0, &abort_flag, err, limit);
 }
 
 int device_sm_count() {
@@ -684,6 +700,14 @@ ca_status ca_dcp_slot_mapping(const int64_t* positions, int64_t n, const int32_t
 }
 
 // ------------------------------------------------------------------ status
+ca_status ca_selftest_wait_timeout(long long limit_cycles, void* stream) {
+  if (limit_cycles <= 0 || limit_cycles > kWaitLimitCycles) return CA_ERR_INVALID_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return CA_ERR_CUDA;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, limit_cycles);
+  return launched(cudaGetLastError());
+}
+
 ca_status ca_device_status(int reset) {
   unsigned* p = device_error_word();
   if (!p) return CA_ERR_CUDA;

@@ -58,19 +58,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // false) when another thread of the block raised *abort, or after
 // kWaitLimitCycles, in which case it raises *abort and flags the device
 // error word.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort, unsigned* err) {
+__device__ __forceinline__ bool mbar_wait_cycles(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                 unsigned* err, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       atomicOr(err, kErrTimeout);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int* abort, unsigned* err) {
+  return mbar_wait_cycles(bar, parity, abort, err, kWaitLimitCycles);
 }
 
 // ----------------------------------------------------------------- TMA

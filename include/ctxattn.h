@@ -476,6 +476,17 @@ ca_status ca_dcp_slot_mapping(const int64_t *positions, int64_t n,
                               int interleave, int64_t *slots);
 
 /* ------------------------------------------------------------------------
+ * Diagnostic of the failure path: launches one warp on `stream` that waits on
+ * an mbarrier nothing ever completes.  Its bounded wait gives up after
+ * `limit_cycles` SM clock cycles and raises the device error word, as a
+ * stalled pipeline's waits would, without any fault.  ca_device_status then
+ * reports CA_ERR_TIMEOUT, and the context stays usable.
+ * Errors: CA_ERR_INVALID_ARG unless 0 < limit_cycles <= the kernels' own
+ * wait limit (4e9 cycles, ~2 s).
+ * ---------------------------------------------------------------------- */
+ca_status ca_selftest_wait_timeout(long long limit_cycles, void *stream);
+
+/* ------------------------------------------------------------------------
  * Device status: reads (synchronously, on the current device) the error word
  * that bounded waits set when they give up, and clears it if `reset`.
  * Returns CA_OK, CA_ERR_TIMEOUT, or CA_ERR_CUDA.

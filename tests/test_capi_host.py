@@ -239,3 +239,10 @@ def test_empty_problems(ca):
                                  FAKE, FAKE, None, None, None)] == "CA_ERR_INVALID_ARG"
     assert S[lib.ca_key_max2(FAKE, 1, 1, 2, 0, 128, FAKE, None)] == "CA_ERR_INVALID_ARG"
     assert S[lib.ca_paged_kv_write(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 0, 2, 128, 4, 64, 16, None)] == "CA_OK"
+
+
+def test_selftest_wait_timeout_validation(ca):
+    lib = ca._load()
+    S = ca.STATUS
+    assert S[lib.ca_selftest_wait_timeout(0, None)] == "CA_ERR_INVALID_ARG"
+    assert S[lib.ca_selftest_wait_timeout(5_000_000_000, None)] == "CA_ERR_INVALID_ARG"  # above the kernels' limit
