@@ -136,7 +136,15 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def dist_setup(n_gpus):
+# a rank that dies leaves the others at their next collective; they give up
+# after this long (the longest gap between collectives is rank 0's CPU
+# baseline, ~16 s) instead of holding every GPU for the backend's default
+PG_TIMEOUT_S = 300
+
+
+def dist_setup(n_gpus, backend="nccl", timeout_s=PG_TIMEOUT_S):
+    import datetime
+
     import torch
 
     rank = int(os.environ.get("RANK", "0"))
@@ -148,8 +156,9 @@ def dist_setup(n_gpus):
     if world > 1:
         import torch.distributed as dist
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend, timeout=datetime.timedelta(seconds=timeout_s))
         pg = dist
     return rank, world, local, pg
 

@@ -78,3 +78,50 @@ def test_rejected_clocks_are_measured_once_more():
     runs.clear()
     r = bench.timed_with_retry(timed([["sw_power_cap"]]), None)
     assert len(runs) == 1 and "remeasured_after" not in r["clocks"]
+
+
+def _worker_one_leaves(rank, world, port, q):
+    import time
+
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    import bench
+
+    _, _, _, pg = bench.dist_setup(world, backend="gloo", timeout_s=5)
+    bench.barrier(pg)  # both ranks are up
+    if rank == 1:
+        q.put((rank, "left"))
+        q.close()
+        q.join_thread()  # the item must reach the pipe before the process vanishes
+        os._exit(3)  # a rank dies between steps, without a word to the others
+    t0 = time.time()
+    try:
+        bench.barrier(pg)
+        q.put((rank, "no error", time.time() - t0))
+    except Exception as e:  # noqa: BLE001 -- the failure is the point
+        q.put((rank, type(e).__name__, time.time() - t0))
+    q.close()
+    q.join_thread()
+    os._exit(0)  # no teardown of a group with a dead member
+
+
+def test_a_rank_that_leaves_is_detected_by_the_others():
+    """A rank that exits between steps makes the survivors' next collective
+    fail within the process group's timeout rather than hang."""
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker_one_leaves, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode is not None, "a rank hung"
+    res = {}
+    for _ in range(world):
+        item = q.get(timeout=10)
+        res[item[0]] = item[1:]
+    assert res[1] == ("left",)
+    outcome, waited = res[0]
+    assert outcome != "no error" and waited < 60.0, res
