@@ -74,11 +74,13 @@ constexpr int kBarQEmpty = kBarQFull + 1;
 constexpr int kBarSFull = kBarQEmpty + 1;   // 2
 constexpr int kBarPFull = kBarSFull + 2;    // 2
 constexpr int kBarOFull = kBarPFull + 2;    // 2
-constexpr int kNumBars = kBarOFull + 2;
+constexpr int kBarDrain = kBarOFull + 2;    // error path: the MMAs issued so far completed
+constexpr int kNumBars = kBarDrain + 1;
 constexpr uint32_t kSmemTmemSlot = kSmemBar + 8 * kNumBars;
 constexpr uint32_t kSmemAbort = kSmemTmemSlot + 4;
 constexpr uint32_t kSmemUsed = kSmemAbort + 4;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // slack for 1024-byte alignment
+static_assert(kSmemAlloc <= 232448, "dynamic shared memory per block");
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // + 128*i
@@ -595,6 +597,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
       mbar_init(bar(kBarPFull + i), kBM);
       mbar_init(bar(kBarOFull + i), 1);
     }
+    mbar_init(bar(kBarDrain), 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -761,6 +764,13 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         }
         gt += n;
         ++uc;
+      }
+      if (!ok) {
+        // error path: MMAs already issued still write TMEM; wait (bounded)
+        // for all of them before the TMEM is freed
+        tc_commit_lane0(bar(kBarDrain));
+        volatile int never = 0;
+        mbar_wait(bar(kBarDrain), 0, &never, err);
       }
     }
   } else {
