@@ -16,8 +16,14 @@ synthetic input:
   q, k, v copied host->device and o copied back inside the timed region, the
   copies of one step overlapping the attention of the previous one.
 
-Both workloads' inputs (0.5 GB and 34 GB) are larger than the 129 MB L2, so
-no flush runs between timed iterations.  ``--impl reference`` times the fp64
+* other_workloads (single-GPU runs; reported, not the value) -- online max,
+  sink keys, causal GQA in both layouts, the QKV prologue, DCP prefill, paged
+  decode and Ring Pass-Q decode, each timed the same way.
+
+SM clocks and throttle reasons are sampled during the timed regions; a region
+that saw a thermal or hardware slowdown is measured once more.  Both headline
+workloads' inputs (0.5 GB and 34 GB) are larger than the 129 MB L2, so no
+flush runs between timed iterations.  ``--impl reference`` times the fp64
 CPU oracle (the only reference this method has) on a bounded sample of the
 same workload.  Under torchrun every rank runs an independent replica (the
 method is not sharded across GPUs on this path) and rank 0 reports the
