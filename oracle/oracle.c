@@ -63,6 +63,7 @@ static int64_t global_pos(int layout, int cp, int64_t Ls, int64_t rho) {
   return r * Ls + a;
 }
 
+/* Exported form of global_pos, for the index-map pins. */
 int64_t ora_global_pos(int layout, int cp, int64_t Ls, int64_t rho) {
   return global_pos(layout, cp, Ls, rho);
 }
