@@ -34,8 +34,9 @@
  *
  * Parity pins: every function here is pinned by the not-gpu tests in
  * tests/test_oracle_pins.py and tests/test_index_maps.py (closed forms,
- * invariants, brute force on tiny inputs, the pages' worked examples).
- * No function is left "parity unpinned".
+ * invariants, brute force on tiny inputs, the pages' worked examples), and
+ * its independent routes are cross-checked on random shapes in
+ * tests/test_oracle_fuzz.py.  No function is left "parity unpinned".
  *
  * Row conventions.  q is [B, Hq, S, D], k and v are [B, Hkv, S, D], all
  * row-major.  The S rows of a head are stored shard-major: row rho = r*Ls + a
