@@ -125,3 +125,17 @@ def test_a_rank_that_leaves_is_detected_by_the_others():
     assert res[1] == ("left",)
     outcome, waited = res[0]
     assert outcome != "no error" and waited < 60.0, res
+
+
+def test_causal_rank_imbalance_closed_forms():
+    """The per-virtual-rank causal work the bench reports: contiguous shards
+    give rank r about (r + 1/2) * Ls keys per query, so max/mean tends to
+    (2 cp - 1) / cp; striped shards split every prefix evenly, ratio -> 1;
+    one shard is balanced by definition."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    for cp in (2, 4, 8):
+        assert bench.causal_rank_imbalance(1 << 16, cp, "contiguous") == pytest.approx((2 * cp - 1) / cp, abs=1e-3)
+        assert bench.causal_rank_imbalance(1 << 16, cp, "striped") == pytest.approx(1.0, abs=1e-3)
+    assert bench.causal_rank_imbalance(1024, 1, "contiguous") == 1.0
