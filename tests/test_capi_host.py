@@ -246,3 +246,27 @@ def test_selftest_wait_timeout_validation(ca):
     S = ca.STATUS
     assert S[lib.ca_selftest_wait_timeout(0, None)] == "CA_ERR_INVALID_ARG"
     assert S[lib.ca_selftest_wait_timeout(5_000_000_000, None)] == "CA_ERR_INVALID_ARG"  # above the kernels' limit
+
+
+def test_no_cpu_fallback(ca):
+    """Host tensors are refused before anything runs: the product path has no
+    CPU implementation to fall back on."""
+    import torch
+
+    q = torch.zeros(1, 2, 256, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ca.ring_attn_fwd(q, q, q, 2)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ca.dcp_decode(torch.zeros(1, 2, 128, dtype=torch.bfloat16), torch.zeros(2, 1, 2, 64, 128, dtype=torch.bfloat16),
+                      torch.zeros(2, 1, 2, 64, 128, dtype=torch.bfloat16), 16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ca.ring_decode(torch.zeros(1, 2, 128, dtype=torch.bfloat16), q, q, 2)
+
+
+def test_missing_library_fails_loudly(ca, monkeypatch):
+    """Without the built library the binding raises instead of computing
+    anything another way."""
+    monkeypatch.setattr(ca, "_lib", None)
+    monkeypatch.setattr(ca, "_LIB_PATH", "/nonexistent/libctxattn.so")
+    with pytest.raises(ca.CtxAttnError):
+        ca._load()
