@@ -192,6 +192,23 @@ def timed_with_retry(timed, pg):
     return res
 
 
+def input_digest(seed, **tensors):
+    """The seed and, per input tensor, the SHA-256 of its first MiB of raw
+    bytes (the whole tensor if smaller), so that two runs can show they drew
+    the same inputs."""
+    import hashlib
+
+    import torch
+
+    out = {"seed": seed}
+    for name, t in tensors.items():
+        flat = t.detach().reshape(-1)
+        n = min(flat.numel(), (1 << 20) // t.element_size())
+        raw = flat[:n].cpu().contiguous().view(torch.uint8).numpy().tobytes()
+        out[f"{name}_sha256_first_MiB"] = hashlib.sha256(raw).hexdigest()
+    return out
+
+
 def max_over_ranks(x, pg):
     """Max of a float over all ranks (the job's time is its slowest rank's)."""
     if pg is None:
@@ -218,6 +235,7 @@ def bench_prefill(ca, torch, steps, warmup, pg, dev_index):
 
     c = PREFILL
     q, k, v = synth.dit_qk(c["B"], c["H"], c["S"], c["D"], seed=c["seed"], device="cuda")
+    digest = input_digest(c["seed"], q=q, k=k, v=v)
     o = torch.empty_like(q)
     lse = torch.empty(c["B"], c["H"], c["S"], device="cuda", dtype=torch.float32)
     kmax2 = torch.empty(c["B"], c["H"], device="cuda", dtype=torch.float32)
@@ -262,6 +280,7 @@ def bench_prefill(ca, torch, steps, warmup, pg, dev_index):
                     bound_ms=statistics.mean([s.elapsed_time(m) for s, m, _ in evs]), clocks=clk.summary())
 
     res = timed_with_retry(timed, pg)
+    res["inputs"] = digest
     assert ca.device_status() == 0
     # e2e: through the public API from pinned host memory.  Every step copies
     # its q, k, v host->device and its o device->host inside the timed region;
@@ -340,6 +359,7 @@ def bench_decode(ca, torch, steps, warmup, pg, dev_index):
 
     c = DECODE
     q, k, v = synth.decode_inputs(c["N"], c["Hq"], c["Hkv"], c["D"], c["W"], c["Lloc"], c["seed"], device="cuda")
+    digest = input_digest(c["seed"], q=q, k=k, v=v)
     o = torch.empty_like(q)
     lse = torch.empty(c["N"], c["Hq"], device="cuda", dtype=torch.float32)
     ws = torch.empty(ca.dcp_decode_workspace_size(c["N"], c["Hq"], c["Hkv"], c["Lloc"], c["D"], c["W"], c["I"]),
@@ -363,6 +383,7 @@ def bench_decode(ca, torch, steps, warmup, pg, dev_index):
         return dict(ms=a.elapsed_time(b) / steps, clocks=clk.summary())
 
     res = timed_with_retry(timed, pg)
+    res["inputs"] = digest
     assert ca.device_status() == 0
     del q, k, v
     torch.cuda.empty_cache()
@@ -638,7 +659,7 @@ def run_ours(args):
         "config": {"workload": "DiT const-max ring self-attention prefill", "B": PREFILL["B"], "H": PREFILL["H"],
                    "S": PREFILL["S"], "D": PREFILL["D"], "cp_size": PREFILL["cp"], "mode": "const_max",
                    "layout": "contiguous", "causal": False, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (no flush)"},
+                   "l2": "inputs larger than L2 (no flush)", "inputs": pre["inputs"]},
         "pct_of_bf16_peak": round(100.0 * value / world / peak, 2),
         "roofline": {"kernel": "ring_tc_kernel", "bound": "tensor", "achieved": round(ring_tflops, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(ring_tflops / peak, 4),
@@ -667,7 +688,7 @@ def run_ours(args):
                                       "frac": round(gbs / peaks["hbm_gbs"], 4),
                                       "traffic": read_traffic("dcp_decode_kernel_131k.txt"),
                                       "peak_source": f"{peak_src} copy bandwidth"},
-                         "clocks": dec["clocks"]}
+                         "clocks": dec["clocks"], "inputs": dec["inputs"]}
     # the other workloads ride along on single-GPU runs (about 20 s more); a
     # failure there is reported in the line rather than losing the line
     if args.other_workloads or (world == 1 and not args.no_other_workloads):

@@ -139,3 +139,38 @@ def test_causal_rank_imbalance_closed_forms():
         assert bench.causal_rank_imbalance(1 << 16, cp, "contiguous") == pytest.approx((2 * cp - 1) / cp, abs=1e-3)
         assert bench.causal_rank_imbalance(1 << 16, cp, "striped") == pytest.approx(1.0, abs=1e-3)
     assert bench.causal_rank_imbalance(1024, 1, "contiguous") == 1.0
+
+
+def test_input_digest_covers_the_first_mib_of_raw_bytes():
+    """The bench records, beside each workload's seed, the SHA-256 of the
+    first MiB of every input: checked against hashlib over the bytes built
+    independently (bf16 bits are the top half of the fp32 bits of values that
+    bf16 holds exactly), only the first MiB counts, and a seed redraws the
+    same inputs."""
+    import hashlib
+
+    import numpy as np
+    import torch
+
+    import bench
+    from context_attention_gb300 import synth
+
+    vals = np.arange(-256, 256, dtype=np.float32)  # at most 8 significant bits: exact in bf16
+    t = torch.from_numpy(vals).to(torch.bfloat16)
+    bits = (vals.view(np.uint32) >> 16).astype("<u2").tobytes()
+    d = bench.input_digest(7, x=t)
+    assert d == {"seed": 7, "x_sha256_first_MiB": hashlib.sha256(bits).hexdigest()}
+
+    big = torch.zeros(3 << 19, dtype=torch.bfloat16)  # 3 MiB
+    ref = bench.input_digest(1, big=big)["big_sha256_first_MiB"]
+    assert ref == hashlib.sha256(bytes(1 << 20)).hexdigest()
+    big[(1 << 19) + 5] = 1.0  # past the first MiB: no change
+    assert bench.input_digest(1, big=big)["big_sha256_first_MiB"] == ref
+    big[5] = 1.0
+    assert bench.input_digest(1, big=big)["big_sha256_first_MiB"] != ref
+
+    a = synth.dit_qk(1, 2, 256, 128, seed=2, device="cpu")
+    b = synth.dit_qk(1, 2, 256, 128, seed=2, device="cpu")
+    da = bench.input_digest(2, q=a[0], k=a[1], v=a[2])
+    assert da == bench.input_digest(2, q=b[0], k=b[1], v=b[2])
+    assert da != bench.input_digest(2, q=a[1], k=a[0], v=a[2])
