@@ -128,13 +128,54 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _need(t: torch.Tensor, name: str, ndim: int):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
-    if t.dim() != ndim or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
-    if t.dtype not in DTYPE:
-        raise ValueError(f"{name}: dtype {t.dtype} not supported (bf16 or fp32)")
+FLOATS = tuple(DTYPE)
+
+
+def _dims(t, name: str, ndim: int):
+    """Shape of the tensor that fixes a call's problem sizes."""
+    if not isinstance(t, torch.Tensor) or t.dim() != ndim:
+        raise ValueError(f"{name} must be a {ndim}-d tensor")
+    return tuple(t.shape)
+
+
+def _args(*specs):
+    """Check every tensor of one call before anything is launched.
+
+    A spec is (tensor or None, name, shape, dtypes).  shape is a tuple whose
+    None entries match any size, an int (that many elements, any shape) or
+    None (unchecked); dtypes is one dtype, a tuple of them or None (any).  A
+    None tensor is an optional operand left out and is skipped.  First the shapes and
+    dtypes (the kernels read and write exactly the extents the sizes passed
+    to the library give, so a mismatch would run past a buffer), then that
+    all of them are contiguous CUDA tensors on one device."""
+    given = [s for s in specs if s[0] is not None]
+    for t, name, shape, dtypes in given:
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"{name} must be a torch.Tensor")
+        if isinstance(shape, int):
+            if t.numel() != shape:
+                raise ValueError(f"{name}: {t.numel()} elements, expected {shape}")
+        elif shape is not None:
+            if t.dim() != len(shape) or any(e is not None and e != n for e, n in zip(shape, t.shape)):
+                want = "[" + ", ".join("*" if e is None else str(e) for e in shape) + "]"
+                raise ValueError(f"{name}: shape {list(t.shape)}, expected {want}")
+        dts = () if dtypes is None else dtypes if isinstance(dtypes, tuple) else (dtypes,)
+        if dts and t.dtype not in dts:
+            raise ValueError(f"{name}: dtype {t.dtype}, expected {' or '.join(str(d) for d in dts)}")
+    dev = None
+    for t, name, _, _ in given:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the other operands on {dev}")
+
+
+def _ws_bytes(workspace) -> int:
+    return 0 if workspace is None else workspace.numel() * workspace.element_size()
 
 
 def ring_attn_fwd_workspace_size(B, Hq, Hkv, S, D, cp_size, mode="online_max") -> int:
@@ -149,10 +190,11 @@ def ring_attn_fwd(q, k, v, cp_size, mode="online_max", causal=False, layout="con
     q [B,Hq,S,D], k/v [B,Hkv,S,D] (bf16 with D=128, or fp32 with D<=128).
     Returns (o, lse) with o [B,Hq,S,D] in q's dtype and lse [B,Hq,S] fp32."""
     lib = _load()
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _need(t, n, 4)
-    B, Hq, S, D = q.shape
-    Hkv = k.shape[1]
+    B, Hq, S, D = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[1]
+    _args((q, "q", None, FLOATS), (k, "k", (B, Hkv, S, D), q.dtype), (v, "v", (B, Hkv, S, D), q.dtype),
+          (out, "out", (B, Hq, S, D), q.dtype), (lse if return_lse else None, "lse", (B, Hq, S), torch.float32),
+          (workspace, "workspace", None, None))
     if out is None:
         out = torch.empty_like(q)
     if return_lse and lse is None:
@@ -164,7 +206,7 @@ def ring_attn_fwd(q, k, v, cp_size, mode="online_max", causal=False, layout="con
                               DTYPE[q.dtype], B, Hq, Hkv, S, D, cp_size, MODE[mode], int(bool(causal)),
                               LAYOUT[layout], float(softmax_scale or 0.0),
                               _ptr(workspace) if ws_bytes else None,
-                              workspace.numel() if ws_bytes else 0, _stream(q))
+                              _ws_bytes(workspace) if ws_bytes else 0, _stream(q))
     _check("ca_ring_attn_fwd", st)
     return out, (lse if return_lse else None)
 
@@ -173,15 +215,17 @@ def ring_attn_fwd_bounded(q, k, v, c, cp_size, causal=False, layout="contiguous"
                           out=None, lse=None, return_lse=True):
     """Const-max ring attention with a caller-provided bound c [B,Hq,S] fp32."""
     lib = _load()
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _need(t, n, 4)
-    B, Hq, S, D = q.shape
-    Hkv = k.shape[1]
+    B, Hq, S, D = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[1]
+    c = c.contiguous() if isinstance(c, torch.Tensor) else c
+    _args((q, "q", None, FLOATS), (k, "k", (B, Hkv, S, D), q.dtype), (v, "v", (B, Hkv, S, D), q.dtype),
+          (c, "c", (B, Hq, S), torch.float32), (out, "out", (B, Hq, S, D), q.dtype),
+          (lse if return_lse else None, "lse", (B, Hq, S), torch.float32))
     if out is None:
         out = torch.empty_like(q)
     if return_lse and lse is None:
         lse = torch.empty(B, Hq, S, device=q.device, dtype=torch.float32)
-    st = lib.ca_ring_attn_fwd_bounded(_ptr(q), _ptr(k), _ptr(v), _ptr(c.contiguous()), _ptr(out),
+    st = lib.ca_ring_attn_fwd_bounded(_ptr(q), _ptr(k), _ptr(v), _ptr(c), _ptr(out),
                                       _ptr(lse if return_lse else None), DTYPE[q.dtype], B, Hq, Hkv, S, D,
                                       cp_size, int(bool(causal)), LAYOUT[layout], float(softmax_scale or 0.0),
                                       _stream(q))
@@ -195,15 +239,17 @@ def ring_attn_fwd_kmax(q, k, v, kmax2, cp_size, causal=False, layout="contiguous
     [B,Hkv] fp32 (max |k_j|^2 per head, e.g. from key_max2, or its max over
     processes); each row's bound is formed in the kernel."""
     lib = _load()
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _need(t, n, 4)
-    B, Hq, S, D = q.shape
-    Hkv = k.shape[1]
+    B, Hq, S, D = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[1]
+    kmax2 = kmax2.contiguous() if isinstance(kmax2, torch.Tensor) else kmax2
+    _args((q, "q", None, FLOATS), (k, "k", (B, Hkv, S, D), q.dtype), (v, "v", (B, Hkv, S, D), q.dtype),
+          (kmax2, "kmax2", (B, Hkv), torch.float32), (out, "out", (B, Hq, S, D), q.dtype),
+          (lse if return_lse else None, "lse", (B, Hq, S), torch.float32))
     if out is None:
         out = torch.empty_like(q)
     if return_lse and lse is None:
         lse = torch.empty(B, Hq, S, device=q.device, dtype=torch.float32)
-    st = lib.ca_ring_attn_fwd_kmax(_ptr(q), _ptr(k), _ptr(v), _ptr(kmax2.contiguous()), _ptr(out),
+    st = lib.ca_ring_attn_fwd_kmax(_ptr(q), _ptr(k), _ptr(v), _ptr(kmax2), _ptr(out),
                                    _ptr(lse if return_lse else None), DTYPE[q.dtype], B, Hq, Hkv, S, D,
                                    cp_size, int(bool(causal)), LAYOUT[layout], float(softmax_scale or 0.0),
                                    _stream(q))
@@ -218,14 +264,14 @@ def attn_partial_step(q_shard, k_shard, v_shard, q_rank, kv_rank, cp_size, mode=
     Returns (o_part fp32, lse_part fp32).  In const-max mode pass the shard's
     rows of the bound c; o_part is then the unnormalised sum."""
     lib = _load()
-    for n, t in (("q_shard", q_shard), ("k_shard", k_shard), ("v_shard", v_shard)):
-        _need(t, n, 4)
-    B, Hq, Ls, D = q_shard.shape
-    Hkv = k_shard.shape[1]
+    B, Hq, Ls, D = _dims(q_shard, "q_shard", 4)
+    Hkv = _dims(k_shard, "k_shard", 4)[1]
+    if isinstance(c, torch.Tensor):
+        c = c.contiguous()
+    _args((q_shard, "q_shard", None, FLOATS), (k_shard, "k_shard", (B, Hkv, Ls, D), q_shard.dtype),
+          (v_shard, "v_shard", (B, Hkv, Ls, D), q_shard.dtype), (c, "c", (B, Hq, Ls), torch.float32))
     o = torch.empty(B, Hq, Ls, D, device=q_shard.device, dtype=torch.float32)
     lse = torch.empty(B, Hq, Ls, device=q_shard.device, dtype=torch.float32)
-    if c is not None:
-        c = c.contiguous()
     st = lib.ca_attn_partial_step(_ptr(q_shard), _ptr(k_shard), _ptr(v_shard), DTYPE[q_shard.dtype],
                                   B, Hq, Hkv, Ls, D, q_rank, kv_rank, cp_size, MODE[mode],
                                   int(bool(causal)), LAYOUT[layout], float(softmax_scale or 0.0),
@@ -237,15 +283,20 @@ def attn_partial_step(q_shard, k_shard, v_shard, q_rank, kv_rank, cp_size, mode=
 def lse_merge(o_parts, lse_parts, c=None, out_dtype=torch.float32):
     """Merge n partials o_parts [n, ..., D], lse_parts [n, ...] (fp32)."""
     lib = _load()
-    if not (o_parts.is_cuda and o_parts.dtype == torch.float32 and o_parts.is_contiguous()):
-        raise ValueError("o_parts must be a contiguous CUDA fp32 tensor")
+    if not isinstance(o_parts, torch.Tensor) or o_parts.dim() < 2:
+        raise ValueError("o_parts must be a tensor [n, ..., D]")
+    if out_dtype not in DTYPE:
+        raise ValueError(f"out_dtype {out_dtype} not supported (bf16 or fp32)")
     n, D = o_parts.shape[0], o_parts.shape[-1]
-    R = o_parts[0].numel() // D
-    lse_parts = lse_parts.contiguous()
+    R = o_parts[0].numel() // D if D else 0
+    lse_parts = lse_parts.contiguous() if isinstance(lse_parts, torch.Tensor) else lse_parts
+    c = c.contiguous() if isinstance(c, torch.Tensor) else c
+    _args((o_parts, "o_parts", None, torch.float32), (lse_parts, "lse_parts", tuple(o_parts.shape[:-1]), torch.float32),
+          (c, "c", R, torch.float32))
     o = torch.empty(o_parts.shape[1:], device=o_parts.device, dtype=out_dtype)
     lse = torch.empty(o_parts.shape[1:-1], device=o_parts.device, dtype=torch.float32)
     st = lib.ca_lse_merge(_ptr(o_parts), _ptr(lse_parts), n, R, D,
-                          _ptr(c.contiguous()) if c is not None else None, _ptr(o), DTYPE[out_dtype],
+                          _ptr(c), _ptr(o), DTYPE[out_dtype],
                           _ptr(lse), _stream(o_parts))
     _check("ca_lse_merge", st)
     return o, lse
@@ -259,10 +310,15 @@ def qkv_prologue(x_q, x_k, Hq, Hkv, x_v=None, g_q=None, g_k=None, eps=1e-6, rope
     in the shard-major row order of the layout.  Returns (q, k, v or None,
     kmax2 [B,Hkv] or None)."""
     lib = _load()
-    _need(x_q, "x_q", 3)
-    _need(x_k, "x_k", 3)
-    B, S, HqD = x_q.shape
+    B, S, HqD = _dims(x_q, "x_q", 3)
+    if Hq <= 0 or Hkv <= 0 or HqD % Hq:
+        raise ValueError(f"x_q's last dimension {HqD} is not Hq={Hq} heads")
     D = HqD // Hq
+    if (rope_cos is None) != (rope_sin is None):
+        raise ValueError("rope_cos and rope_sin go together")
+    _args((x_q, "x_q", None, FLOATS), (x_k, "x_k", (B, S, Hkv * D), x_q.dtype), (x_v, "x_v", (B, S, Hkv * D), x_q.dtype),
+          (g_q, "g_q", Hq * D, torch.float32), (g_k, "g_k", Hkv * D, torch.float32),
+          (rope_cos, "rope_cos", S * (D // 2), torch.float32), (rope_sin, "rope_sin", S * (D // 2), torch.float32))
     q = torch.empty(B, Hq, S, D, device=x_q.device, dtype=x_q.dtype)
     k = torch.empty(B, Hkv, S, D, device=x_q.device, dtype=x_q.dtype)
     v = None if x_v is None else torch.empty(B, Hkv, S, D, device=x_q.device, dtype=x_q.dtype)
@@ -277,8 +333,8 @@ def qkv_prologue(x_q, x_k, Hq, Hkv, x_v=None, g_q=None, g_k=None, eps=1e-6, rope
 def key_max2(k, out=None):
     """kmax2 [B,Hkv] fp32: per head, the max over keys of |k_j|^2."""
     lib = _load()
-    _need(k, "k", 4)
-    B, Hkv, S, D = k.shape
+    B, Hkv, S, D = _dims(k, "k", 4)
+    _args((k, "k", None, FLOATS), (out, "out", (B, Hkv), torch.float32))
     if out is None:
         out = torch.empty(B, Hkv, device=k.device, dtype=torch.float32)
     st = lib.ca_key_max2(_ptr(k), DTYPE[k.dtype], B, Hkv, S, D, _ptr(out), _stream(k))
@@ -289,10 +345,9 @@ def key_max2(k, out=None):
 def const_max_bound(q, k, softmax_scale=None):
     """Per-row const-max bound: returns (c [B,Hq,S] fp32, kmax2 [B,Hkv] fp32)."""
     lib = _load()
-    _need(q, "q", 4)
-    _need(k, "k", 4)
-    B, Hq, S, D = q.shape
-    Hkv = k.shape[1]
+    B, Hq, S, D = _dims(q, "q", 4)
+    Hkv = _dims(k, "k", 4)[1]
+    _args((q, "q", None, FLOATS), (k, "k", (B, Hkv, S, D), q.dtype))
     c = torch.empty(B, Hq, S, device=q.device, dtype=torch.float32)
     kmax2 = torch.empty(B, Hkv, device=q.device, dtype=torch.float32)
     st = lib.ca_const_max_bound(_ptr(q), _ptr(k), DTYPE[q.dtype], B, Hq, Hkv, S, D,
@@ -317,11 +372,12 @@ def dcp_decode(q, k_shards, v_shards, interleave, seq_lens=None, softmax_scale=N
 
     seq_lens: optional CUDA int32 [N].  Returns (o [N,Hq,D], lse [N,Hq])."""
     lib = _load()
-    _need(q, "q", 3)
-    _need(k_shards, "k_shards", 5)
-    _need(v_shards, "v_shards", 5)
-    N, Hq, D = q.shape
-    W, _, Hkv, Lloc, _ = k_shards.shape
+    N, Hq, D = _dims(q, "q", 3)
+    W, _, Hkv, Lloc, _ = _dims(k_shards, "k_shards", 5)
+    _args((q, "q", None, FLOATS), (k_shards, "k_shards", (W, N, Hkv, Lloc, D), q.dtype),
+          (v_shards, "v_shards", (W, N, Hkv, Lloc, D), q.dtype), (seq_lens, "seq_lens", (N,), torch.int32),
+          (out, "out", (N, Hq, D), q.dtype), (lse, "lse", (N, Hq), torch.float32),
+          (workspace, "workspace", None, None))
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -329,12 +385,9 @@ def dcp_decode(q, k_shards, v_shards, interleave, seq_lens=None, softmax_scale=N
     ws_bytes = int(lib.ca_dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, W, interleave))
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), device=q.device, dtype=torch.uint8)
-    if seq_lens is not None:
-        if not (seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()):
-            raise ValueError("seq_lens must be a contiguous CUDA int32 tensor")
     st = lib.ca_dcp_decode(_ptr(q), _ptr(k_shards), _ptr(v_shards), DTYPE[q.dtype], N, Hq, Hkv, Lloc,
                            D, W, interleave, _ptr(seq_lens), float(softmax_scale or 0.0), _ptr(out),
-                           _ptr(lse), _ptr(workspace), workspace.numel(), _stream(q))
+                           _ptr(lse), _ptr(workspace), _ws_bytes(workspace), _stream(q))
     _check("ca_dcp_decode", st)
     return out, lse
 
@@ -347,11 +400,11 @@ def ring_decode(q, k, v, cp_size, layout="contiguous", seq_lens=None, softmax_sc
     seq_lens: optional CUDA int32 [B] (cached tokens, default S).  Returns
     (o [B,Hq,D], lse [B,Hq])."""
     lib = _load()
-    _need(q, "q", 3)
-    _need(k, "k", 4)
-    _need(v, "v", 4)
-    B, Hq, D = q.shape
-    _, Hkv, S, _ = k.shape
+    B, Hq, D = _dims(q, "q", 3)
+    _, Hkv, S, _ = _dims(k, "k", 4)
+    _args((q, "q", None, FLOATS), (k, "k", (B, Hkv, S, D), q.dtype), (v, "v", (B, Hkv, S, D), q.dtype),
+          (seq_lens, "seq_lens", (B,), torch.int32), (out, "out", (B, Hq, D), q.dtype),
+          (lse, "lse", (B, Hq), torch.float32), (workspace, "workspace", None, None))
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -359,12 +412,9 @@ def ring_decode(q, k, v, cp_size, layout="contiguous", seq_lens=None, softmax_sc
     ws_bytes = int(lib.ca_ring_decode_workspace_size(B, Hq, Hkv, S, D, cp_size))
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), device=q.device, dtype=torch.uint8)
-    if seq_lens is not None:
-        if not (seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()):
-            raise ValueError("seq_lens must be a contiguous CUDA int32 tensor")
     st = lib.ca_ring_decode(_ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, Hq, Hkv, S, D, cp_size, LAYOUT[layout],
                             _ptr(seq_lens), float(softmax_scale or 0.0), _ptr(out), _ptr(lse), _ptr(workspace),
-                            workspace.numel(), _stream(q))
+                            _ws_bytes(workspace), _stream(q))
     _check("ca_ring_decode", st)
     return out, lse
 
@@ -380,11 +430,11 @@ def dcp_decode_noalloc(q, k_shards, v_shards, interleave, seq_lens=None, softmax
     this call free of allocations on the Python side too.  Larger problems
     raise CtxAttnError (CA_ERR_WORKSPACE)."""
     lib = _load()
-    _need(q, "q", 3)
-    _need(k_shards, "k_shards", 5)
-    _need(v_shards, "v_shards", 5)
-    N, Hq, D = q.shape
-    W, _, Hkv, Lloc, _ = k_shards.shape
+    N, Hq, D = _dims(q, "q", 3)
+    W, _, Hkv, Lloc, _ = _dims(k_shards, "k_shards", 5)
+    _args((q, "q", None, FLOATS), (k_shards, "k_shards", (W, N, Hkv, Lloc, D), q.dtype),
+          (v_shards, "v_shards", (W, N, Hkv, Lloc, D), q.dtype), (seq_lens, "seq_lens", (N,), torch.int32),
+          (out, "out", (N, Hq, D), q.dtype), (lse, "lse", (N, Hq), torch.float32))
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -401,15 +451,16 @@ def dcp_decode_paged(q, k_cache, v_cache, block_tables, interleave, seq_lens, so
     """DCP decode over paged caches.  q [N,Hq,D]; k/v cache [dcp,nblk,Hkv,bs,D];
     block_tables CUDA int32 [dcp,N,max_blocks]; seq_lens CUDA int32 [N]."""
     lib = _load()
-    _need(q, "q", 3)
-    _need(k_cache, "k_cache", 5)
-    _need(v_cache, "v_cache", 5)
-    N, Hq, D = q.shape
-    W, nblk, Hkv, bs, _ = k_cache.shape
-    max_blocks = block_tables.shape[2]
-    for name, t in (("block_tables", block_tables), ("seq_lens", seq_lens)):
-        if not (t.is_cuda and t.dtype == torch.int32 and t.is_contiguous()):
-            raise ValueError(f"{name} must be a contiguous CUDA int32 tensor")
+    N, Hq, D = _dims(q, "q", 3)
+    W, nblk, Hkv, bs, _ = _dims(k_cache, "k_cache", 5)
+    max_blocks = _dims(block_tables, "block_tables", 3)[2]
+    if seq_lens is None:
+        raise ValueError("seq_lens is required for the paged cache")
+    _args((q, "q", None, FLOATS), (k_cache, "k_cache", (W, nblk, Hkv, bs, D), q.dtype),
+          (v_cache, "v_cache", (W, nblk, Hkv, bs, D), q.dtype),
+          (block_tables, "block_tables", (W, N, max_blocks), torch.int32), (seq_lens, "seq_lens", (N,), torch.int32),
+          (out, "out", (N, Hq, D), q.dtype), (lse, "lse", (N, Hq), torch.float32),
+          (workspace, "workspace", None, None))
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -420,7 +471,7 @@ def dcp_decode_paged(q, k_cache, v_cache, block_tables, interleave, seq_lens, so
     st = lib.ca_dcp_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), DTYPE[q.dtype], N, Hq,
                                  Hkv, nblk, bs, max_blocks, D, W, interleave, _ptr(seq_lens),
                                  float(softmax_scale or 0.0), _ptr(out), _ptr(lse), _ptr(workspace),
-                                 workspace.numel(), _stream(q))
+                                 _ws_bytes(workspace), _stream(q))
     _check("ca_dcp_decode_paged", st)
     return out, lse
 
@@ -428,13 +479,26 @@ def dcp_decode_paged(q, k_cache, v_cache, block_tables, interleave, seq_lens, so
 def paged_kv_write(k_new, v_new, slots, k_cache, v_cache):
     """Write new tokens' K/V [T,Hkv,D] into the paged caches by slot mapping
     (slots: CUDA int64 [dcp, T], -1 = not owned)."""
-    T, Hkv, D = k_new.shape
-    W, nblk, _, bs, _ = k_cache.shape
-    if not (slots.is_cuda and slots.dtype == torch.int64 and slots.is_contiguous()):
-        raise ValueError("slots must be a contiguous CUDA int64 tensor")
+    T, Hkv, D = _dims(k_new, "k_new", 3)
+    W, nblk, _, bs, _ = _dims(k_cache, "k_cache", 5)
+    _args((k_new, "k_new", None, FLOATS), (v_new, "v_new", (T, Hkv, D), k_new.dtype),
+          (slots, "slots", (W, T), torch.int64), (k_cache, "k_cache", (W, nblk, Hkv, bs, D), k_new.dtype),
+          (v_cache, "v_cache", (W, nblk, Hkv, bs, D), k_new.dtype))
     st = _load().ca_paged_kv_write(_ptr(k_new), _ptr(v_new), _ptr(slots), _ptr(k_cache), _ptr(v_cache),
                                    DTYPE[k_new.dtype], T, Hkv, D, W, nblk, bs, _stream(k_new))
     _check("ca_paged_kv_write", st)
+
+
+def _prefill_dims(q, k_prior, v_prior, k_cur, v_cur, out=None, lse=None):
+    """Sizes of a DCP prefill call, after checking its tensors."""
+    Hq, Sc, D = _dims(q, "q", 3)
+    W, Hkv, Lcap, _ = _dims(k_prior, "k_prior", 4)
+    Lc = _dims(k_cur, "k_cur", 4)[2]
+    _args((q, "q", None, FLOATS), (k_prior, "k_prior", (W, Hkv, Lcap, D), q.dtype),
+          (v_prior, "v_prior", (W, Hkv, Lcap, D), q.dtype), (k_cur, "k_cur", (W, Hkv, Lc, D), q.dtype),
+          (v_cur, "v_cur", (W, Hkv, Lc, D), q.dtype), (out, "out", (Hq, Sc, D), q.dtype),
+          (lse, "lse", (Hq, Sc), torch.float32))
+    return Hq, Sc, D, W, Hkv, Lcap, Lc
 
 
 def dcp_prefill(q, k_prior, v_prior, k_cur, v_cur, interleave, prior_tokens, softmax_scale=None, out=None,
@@ -444,12 +508,7 @@ def dcp_prefill(q, k_prior, v_prior, k_cur, v_cur, interleave, prior_tokens, sof
     q [Hq,Sc,D]; prior shards [dcp,Hkv,Lcap,D]; current shards [dcp,Hkv,Lc,D]
     (bf16, D=128).  Returns (o [Hq,Sc,D] bf16, lse [Hq,Sc])."""
     lib = _load()
-    _need(q, "q", 3)
-    for n, t in (("k_prior", k_prior), ("v_prior", v_prior), ("k_cur", k_cur), ("v_cur", v_cur)):
-        _need(t, n, 4)
-    Hq, Sc, D = q.shape
-    W, Hkv, Lcap, _ = k_prior.shape
-    Lc = k_cur.shape[2]
+    Hq, Sc, D, W, Hkv, Lcap, Lc = _prefill_dims(q, k_prior, v_prior, k_cur, v_cur, out, lse)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -464,10 +523,7 @@ def dcp_prefill(q, k_prior, v_prior, k_cur, v_cur, interleave, prior_tokens, sof
 def dcp_prefill_partial(q, k_prior, v_prior, k_cur, v_cur, interleave, prior_tokens, rank, softmax_scale=None):
     """One rank's DCP prefill partial: (o_part [Hq,Sc,D] fp32, lse_part [Hq,Sc])."""
     lib = _load()
-    _need(q, "q", 3)
-    Hq, Sc, D = q.shape
-    W, Hkv, Lcap, _ = k_prior.shape
-    Lc = k_cur.shape[2]
+    Hq, Sc, D, W, Hkv, Lcap, Lc = _prefill_dims(q, k_prior, v_prior, k_cur, v_cur)
     o = torch.empty(Hq, Sc, D, device=q.device, dtype=torch.float32)
     lse = torch.empty(Hq, Sc, device=q.device, dtype=torch.float32)
     st = lib.ca_dcp_prefill_partial(_ptr(q), _ptr(k_prior), _ptr(v_prior), _ptr(k_cur), _ptr(v_cur),
