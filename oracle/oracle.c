@@ -46,6 +46,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
@@ -54,6 +55,17 @@
 
 #define ORA_LAYOUT_CONTIGUOUS 0
 #define ORA_LAYOUT_STRIPED 1
+
+/* Zero-filled allocation that stops the process with a message when memory
+ * runs out, so that a failed allocation can never pass for a result. */
+static void *ora_alloc(size_t count, size_t size) {
+  void *p = calloc(count ? count : 1, size);
+  if (!p) {
+    fprintf(stderr, "oracle: out of memory (%zu x %zu bytes)\n", count, size);
+    abort();
+  }
+  return p;
+}
 
 /* Global token position of stored row rho (see the row conventions above).
  * Contiguous: shard r holds tokens [r*Ls, (r+1)*Ls) in order.
@@ -78,7 +90,7 @@ static void attend_row(const float *qrow, const float *kh, const float *vh,
                        double *orow, double *lse_out) {
   int64_t Ls = S / cp;
   int64_t qpos = global_pos(layout, cp, Ls, qrho);
-  double *s = (double *)malloc(sizeof(double) * (size_t)(k_end - k_begin + 1));
+  double *s = (double *)ora_alloc((size_t)(k_end - k_begin + 1), sizeof(double));
   double m = -INFINITY;
   for (int64_t j = k_begin; j < k_end; ++j) {
     int allowed = 1;
@@ -260,8 +272,8 @@ void ora_ring_rows(const float *q, const float *k, const float *v, int B,
     int64_t qpos = global_pos(layout, cp, Ls, rho);
     double *orow = o + i * D;
     if (mode == 0) {
-      double *op = (double *)malloc(sizeof(double) * (size_t)cp * D);
-      double *lp = (double *)malloc(sizeof(double) * (size_t)cp);
+      double *op = (double *)ora_alloc((size_t)cp * D, sizeof(double));
+      double *lp = (double *)ora_alloc((size_t)cp, sizeof(double));
       for (int t = 0; t < cp; ++t) {
         int s = ((r - t) % cp + cp) % cp;
         attend_row(qrow, kh, vh, S, D, scale, causal, layout, cp, rho,
@@ -326,7 +338,7 @@ void ora_ring_rows(const float *q, const float *k, const float *v, int B,
 /* For global positions 0..n-1: owner rank and local index on that rank. */
 void ora_dcp_deal(int64_t n, int W, int I, int32_t *owner, int64_t *local) {
   int rank = 0, in_block = 0;
-  int64_t *count = (int64_t *)calloc((size_t)W, sizeof(int64_t));
+  int64_t *count = (int64_t *)ora_alloc((size_t)W, sizeof(int64_t));
   for (int64_t p = 0; p < n; ++p) {
     owner[p] = rank;
     local[p] = count[rank]++;
@@ -340,8 +352,8 @@ void ora_dcp_deal(int64_t n, int W, int I, int32_t *owner, int64_t *local) {
 
 /* Number of tokens among positions 0..N-1 that rank R holds. */
 int64_t ora_dcp_local_filled(int64_t N, int W, int I, int R) {
-  int32_t *own = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
-  int64_t *loc = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
+  int32_t *own = (int32_t *)ora_alloc((size_t)(N > 0 ? N : 1), sizeof(int32_t));
+  int64_t *loc = (int64_t *)ora_alloc((size_t)(N > 0 ? N : 1), sizeof(int64_t));
   ora_dcp_deal(N, W, I, own, loc);
   int64_t cnt = 0;
   for (int64_t p = 0; p < N; ++p) cnt += own[p] == R;
@@ -368,11 +380,11 @@ void ora_dcp_decode(const float *q, const float *k_shards,
     int64_t L = seq_lens[n];
     const float *qrow = q + nh * D;
     /* which local slots of each rank are valid: deal positions 0..L-1 */
-    int32_t *own = (int32_t *)malloc(sizeof(int32_t) * (size_t)(L > 0 ? L : 1));
-    int64_t *loc = (int64_t *)malloc(sizeof(int64_t) * (size_t)(L > 0 ? L : 1));
+    int32_t *own = (int32_t *)ora_alloc((size_t)(L > 0 ? L : 1), sizeof(int32_t));
+    int64_t *loc = (int64_t *)ora_alloc((size_t)(L > 0 ? L : 1), sizeof(int64_t));
     ora_dcp_deal(L, W, I, own, loc);
-    double *op = (double *)calloc((size_t)W * D, sizeof(double));
-    double *lp = (double *)malloc(sizeof(double) * (size_t)W);
+    double *op = (double *)ora_alloc((size_t)W * D, sizeof(double));
+    double *lp = (double *)ora_alloc((size_t)W, sizeof(double));
     for (int r = 0; r < W; ++r) {
       const float *kh = k_shards + (((int64_t)r * N + n) * Hkv + hk) * Lloc * D;
       const float *vh = v_shards + (((int64_t)r * N + n) * Hkv + hk) * Lloc * D;
@@ -430,8 +442,8 @@ void ora_ring_decode(const float *q, const float *k, const float *v, int B, int 
     const float *qrow = q + bh * D;
     const float *kh = k + ((int64_t)b * Hkv + hk) * S * D;
     const float *vh = v + ((int64_t)b * Hkv + hk) * S * D;
-    double *op = (double *)calloc((size_t)cp * D, sizeof(double));
-    double *lp = (double *)malloc(sizeof(double) * (size_t)cp);
+    double *op = (double *)ora_alloc((size_t)cp * D, sizeof(double));
+    double *lp = (double *)ora_alloc((size_t)cp, sizeof(double));
     for (int r = 0; r < cp; ++r) {
       double m = -INFINITY;
       for (int64_t rho = r * Ls; rho < (r + 1) * Ls; ++rho) {
@@ -486,10 +498,10 @@ void ora_dcp_prefill(const float *q, const float *k_prior, const float *v_prior,
                      int64_t Lc, double scale, int part_rank, const int64_t *rows,
                      int64_t nrows, double *o, double *lse) {
   int G = Hq / Hkv;
-  int32_t *own_p = (int32_t *)malloc(sizeof(int32_t) * (size_t)(P > 0 ? P : 1));
-  int64_t *loc_p = (int64_t *)malloc(sizeof(int64_t) * (size_t)(P > 0 ? P : 1));
-  int32_t *own_c = (int32_t *)malloc(sizeof(int32_t) * (size_t)(Sc > 0 ? Sc : 1));
-  int64_t *loc_c = (int64_t *)malloc(sizeof(int64_t) * (size_t)(Sc > 0 ? Sc : 1));
+  int32_t *own_p = (int32_t *)ora_alloc((size_t)(P > 0 ? P : 1), sizeof(int32_t));
+  int64_t *loc_p = (int64_t *)ora_alloc((size_t)(P > 0 ? P : 1), sizeof(int64_t));
+  int32_t *own_c = (int32_t *)ora_alloc((size_t)(Sc > 0 ? Sc : 1), sizeof(int32_t));
+  int64_t *loc_c = (int64_t *)ora_alloc((size_t)(Sc > 0 ? Sc : 1), sizeof(int64_t));
   ora_dcp_deal(P, W, I, own_p, loc_p);
   ora_dcp_deal(Sc, W, I, own_c, loc_c);
 #pragma omp parallel for schedule(dynamic, 1)
@@ -497,8 +509,8 @@ void ora_dcp_prefill(const float *q, const float *k_prior, const float *v_prior,
     const int64_t hi = rows[ri];
     int64_t h = hi / Sc, i = hi % Sc, hk = h / G;
     const float *qrow = q + hi * D;
-    double *op = (double *)calloc((size_t)W * D, sizeof(double));
-    double *lp = (double *)malloc(sizeof(double) * (size_t)W);
+    double *op = (double *)ora_alloc((size_t)W * D, sizeof(double));
+    double *lp = (double *)ora_alloc((size_t)W, sizeof(double));
     for (int r = 0; r < W; ++r) {
       lp[r] = -INFINITY;
       if (part_rank >= 0 && r != part_rank) continue;
@@ -568,13 +580,13 @@ void ora_dcp_decode_paged(const float *q, const float *k_cache, const float *v_c
                           int bs, int64_t max_blocks, int D, int W, int I,
                           const int64_t *seq_lens, double scale, double *o, double *lse) {
   int64_t Lloc = max_blocks * bs;
-  float *ks = (float *)calloc((size_t)W * N * Hkv * Lloc * D, sizeof(float));
-  float *vs = (float *)calloc((size_t)W * N * Hkv * Lloc * D, sizeof(float));
+  float *ks = (float *)ora_alloc((size_t)W * N * Hkv * Lloc * D, sizeof(float));
+  float *vs = (float *)ora_alloc((size_t)W * N * Hkv * Lloc * D, sizeof(float));
   for (int r = 0; r < W; ++r)
     for (int n = 0; n < N; ++n) {
       /* only the slots the sequence actually has on this rank are gathered */
-      int32_t *own = (int32_t *)malloc(sizeof(int32_t) * (size_t)(seq_lens[n] > 0 ? seq_lens[n] : 1));
-      int64_t *loc = (int64_t *)malloc(sizeof(int64_t) * (size_t)(seq_lens[n] > 0 ? seq_lens[n] : 1));
+      int32_t *own = (int32_t *)ora_alloc((size_t)(seq_lens[n] > 0 ? seq_lens[n] : 1), sizeof(int32_t));
+      int64_t *loc = (int64_t *)ora_alloc((size_t)(seq_lens[n] > 0 ? seq_lens[n] : 1), sizeof(int64_t));
       ora_dcp_deal(seq_lens[n], W, I, own, loc);
       for (int64_t p = 0; p < seq_lens[n]; ++p) {
         if (own[p] != r) continue;
