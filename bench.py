@@ -21,7 +21,8 @@ synthetic input:
   decode and Ring Pass-Q decode, each timed the same way.
 
 SM clocks and throttle reasons are sampled during the timed regions; a region
-that saw a thermal or hardware slowdown is measured once more.  Both headline
+that saw a thermal or hardware slowdown, or SM clocks well below their maximum
+with no reason given (a leftover clock lock), is measured once more.  Both headline
 workloads' inputs (0.5 GB and 34 GB) are larger than the 129 MB L2, so no
 flush runs between timed iterations.  ``--impl reference`` times the fp64
 CPU oracle (the only reference this method has) on a bounded sample of the
@@ -85,6 +86,11 @@ def read_traffic(name):
     return None
 
 
+# a median SM clock below this fraction of the maximum with none of the
+# sampled throttle reasons active is taken for a clock lock left by someone
+LOW_CLOCK_FRACTION = 0.85
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
 
@@ -138,8 +144,10 @@ class ClockSampler:
         os.unlink(self.path)
         if not sms:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs), "samples": len(sms),
-                "reasons": sorted(reasons)}
+        med, top = statistics.median(sms), max(maxs)
+        if med < LOW_CLOCK_FRACTION * top and not reasons:
+            reasons.add("sm_clock_low_no_reason")  # what a clock lock left behind looks like
+        return {"sm_mhz": med, "sm_max_mhz": top, "samples": len(sms), "reasons": sorted(reasons)}
 
 
 # a rank that dies leaves the others at their next collective; they give up
@@ -176,7 +184,7 @@ def barrier(pg):
 
 # a timed region whose clocks saw one of these is not a valid measurement:
 # it is taken once more (sw_power_cap is normal under load and is kept)
-REJECTED_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+REJECTED_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sm_clock_low_no_reason")
 
 
 def timed_with_retry(timed, pg):

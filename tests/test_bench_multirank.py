@@ -174,3 +174,35 @@ def test_input_digest_covers_the_first_mib_of_raw_bytes():
     da = bench.input_digest(2, q=a[0], k=a[1], v=a[2])
     assert da == bench.input_digest(2, q=b[0], k=b[1], v=b[2])
     assert da != bench.input_digest(2, q=a[1], k=a[0], v=a[2])
+
+
+def test_clock_summary_from_sampled_lines(tmp_path):
+    """The clock record of a timed region, from nvidia-smi's CSV lines (no
+    header, no units): median and maximum SM clock, the throttle reasons seen
+    active, unparsable lines skipped, and a clock far below its maximum with
+    no reason flagged as a leftover lock (which the bench re-measures)."""
+    import bench
+
+    def summary(lines):
+        c = bench.ClockSampler(0)
+        c.path = str(tmp_path / "clk.csv")
+        with open(c.path, "w") as f:
+            f.write("".join(line + "\n" for line in lines))
+        out = c.summary()
+        assert not os.path.exists(c.path)  # the sample file is removed
+        return out
+
+    na, act = "Not Active", "Active"
+    row = lambda sm, *r: ", ".join(["0", str(sm), "2070", "850.00", "0x0"] + list(r))  # noqa: E731
+    s = summary([row(1935, na, na, na, act), row(1950, na, na, na, act), row(1700, na, na, na, na),
+                 "0, [N/A], 2070, 1.0, 0x0, Not Active, Not Active, Not Active, Not Active", "garbage"])
+    assert s == {"sm_mhz": 1935.0, "sm_max_mhz": 2070.0, "samples": 3, "reasons": ["sw_power_cap"]}
+    s = summary([row(2070, na, act, na, na), row(2070, na, na, na, na)])
+    assert s["reasons"] == ["hw_thermal_slowdown"] and s["sm_mhz"] == 2070.0
+    # power-capped low clocks are kept; low clocks with no reason are a lock
+    assert summary([row(1732, na, na, na, act)] * 3)["reasons"] == ["sw_power_cap"]
+    s = summary([row(1200, na, na, na, na)] * 3)
+    assert s["reasons"] == ["sm_clock_low_no_reason"]
+    assert "sm_clock_low_no_reason" in bench.REJECTED_REASONS
+    assert summary([row(1800, na, na, na, na)] * 3)["reasons"] == []  # 0.87 of max: not "well below"
+    assert summary([])["reasons"] == ["unsampled"]
