@@ -206,3 +206,32 @@ def test_clock_summary_from_sampled_lines(tmp_path):
     assert "sm_clock_low_no_reason" in bench.REJECTED_REASONS
     assert summary([row(1800, na, na, na, na)] * 3)["reasons"] == []  # 0.87 of max: not "well below"
     assert summary([])["reasons"] == ["unsampled"]
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    """`bench.py --impl reference` times the oracle (the method's only
+    reference) on the host and prints one JSON line with the contract's keys;
+    a rank other than 0 prints nothing.  The row sample is cut to 64 rows so
+    the test stays short."""
+    import json
+    import types
+
+    import bench
+
+    monkeypatch.setattr(bench.OracleSampler, "rows_for", lambda self, seconds: 64)
+    args = types.SimpleNamespace(steps=2, warmup=1, gpus=1)
+    monkeypatch.setenv("RANK", "1")
+    bench.run_reference(args)
+    assert capsys.readouterr().out == ""
+    monkeypatch.setenv("RANK", "0")
+    bench.run_reference(args)
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["steps"] == 2 and d["warmup"] == 1
+    assert d["higher_is_better"] is True and d["n_gpus"] == 1 and d["vs_baseline"] is None
+    assert d["config"]["workload"] == "DiT const-max ring self-attention prefill"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and "64 query rows" in cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
