@@ -118,6 +118,7 @@ ca_status ca_ring_attn_fwd(const void *q, const void *k, const void *v, void *o,
                            void *stream);
 
 /* Ring attention in const-max mode with a caller-provided bound
+ * ([CM] "Picking a max that is safe without measuring it")
  * c [B,Hq,S] fp32 (device; e.g. from ca_const_max_bound): the same
  * computation as ca_ring_attn_fwd(mode = CA_MODE_CONST_MAX) without the bound
  * pass, for callers that compute or reuse the bound themselves.  Needs no
@@ -438,8 +439,9 @@ ca_status ca_dcp_shard_kv(const void *kv, void *shards, int64_t NH, int64_t L,
  * same closed forms on the device.
  * ---------------------------------------------------------------------- */
 
-/* Global token position of stored row `row` (= r*Ls + a) for `layout`;
- * -1 on bad arguments. */
+/* Global token position of stored row `row` (= r*Ls + a) for `layout`
+ * (contiguous: r*Ls + a, [CP] "Model Implementation"; striped: a*cp + r,
+ * [SHI]); -1 on bad arguments. */
 int64_t ca_layout_global_index(ca_layout layout, int cp_size, int64_t Ls,
                                int64_t row);
 /* Inverse: stored row of global token `token`; -1 on bad arguments. */
@@ -449,9 +451,12 @@ int64_t ca_layout_shard_row(ca_layout layout, int cp_size, int64_t Ls,
  * (rank - step) mod cp_size; -1 on bad arguments. */
 int ca_ring_kv_shard(int rank, int step, int cp_size);
 
-/* Owner rank of global position pos: (pos / interleave) mod dcp. */
+/* Owner rank of global position pos ([DCP] "Active Token Handling and
+ * dcp_active_mask", "Slot Mapping and KV Cache"): (pos / interleave) mod
+ * dcp. */
 int ca_dcp_owner(int64_t pos, int dcp, int interleave);
-/* Local slot of pos on its owner: (pos / (dcp*I))*I + pos % I. */
+/* Local slot of pos on its owner, the inverse of ca_dcp_local_to_global
+ * ([DCP] "Segmented Attention CP"): (pos / (dcp*I))*I + pos % I. */
 int64_t ca_dcp_local_index(int64_t pos, int dcp, int interleave);
 /* Global position of local slot s on rank R ([DCP] "Segmented Attention
  * CP"): (s / I)*(dcp*I) + R*I + s % I. */
