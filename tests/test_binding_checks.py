@@ -158,3 +158,15 @@ def test_workspace_size_counts_bytes(ca):
     assert ca._ws_bytes(z(10, dtype=F32)) == 40
     assert ca._ws_bytes(z(10, dtype=torch.uint8)) == 10
     assert ca._ws_bytes(None) == 0
+
+
+def test_layout_permutations_refuse_host_tensors(ca):
+    """The row permutations move raw rows of any dtype; host tensors and
+    tensors with fewer than three dimensions are refused before any copy."""
+    x = z(2, 4, 64, 128)
+    for fn in (lambda t: ca.layout_to_shards(t, 4, "striped"), lambda t: ca.layout_from_shards(t, 4),
+               lambda t: ca.dcp_shard_kv(t, 4, 16)):
+        with pytest.raises(ValueError, match="contiguous CUDA tensor"):
+            fn(x)
+        with pytest.raises(ValueError, match="contiguous CUDA tensor"):
+            fn(z(64, 128))
