@@ -31,7 +31,10 @@ static unsigned* device_error_word() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   if (!cache[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
+      cudaGetLastError();  // the failed lookup must not surface in a later, unrelated launch check
+      return nullptr;
+    }
     cache[dev] = static_cast<unsigned*>(p);
   }
   return cache[dev];
@@ -75,7 +78,7 @@ static bool trace_enabled() {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static ca_status device_is_gb300() {
+ca_status device_is_gb300() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CA_ERR_CUDA;
   int major = 0, minor = 0;
@@ -109,6 +112,27 @@ static ca_status check_attn_shape(ca_dtype dtype, int B, int Hq, int Hkv, int64_
   if (dtype == CA_DTYPE_F32 && D > 128) return CA_ERR_UNSUPPORTED;
   // TMA coordinates are 32-bit
   if (dtype == CA_DTYPE_BF16 && (int64_t)B * Hq * S >= ((int64_t)1 << 31)) return CA_ERR_UNSUPPORTED;
+  return CA_OK;
+}
+
+// Host checks of a DCP decode call, everything but its workspace, in the
+// order ca_dcp_decode applies them (ca_dcp_decode_noalloc runs the same ones
+// before it looks at its scratch).
+ca_status check_dcp_decode(const void* q, const void* k_shards, const void* v_shards,
+                           ca_dtype dtype, int N, int Hq, int Hkv, int64_t Lloc, int D, int dcp,
+                           int interleave, const int32_t* seq_lens, const void* o,
+                           const float* lse) {
+  if (!q || !k_shards || !v_shards || !o) return CA_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || N <= 0 || Hq <= 0 || Hkv <= 0 || Lloc <= 0 || D <= 0 || dcp <= 0 ||
+      interleave <= 0)
+    return CA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || Lloc % interleave != 0) return CA_ERR_SHAPE;
+  if (dtype != CA_DTYPE_BF16 || D != 128 || Hq / Hkv > 8) return CA_ERR_UNSUPPORTED;
+  if ((int64_t)dcp * N * Hkv * Lloc >= ((int64_t)1 << 31)) return CA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_shards) || !aligned16(v_shards) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
+      (seq_lens && (reinterpret_cast<uintptr_t>(seq_lens) & 3u)))
+    return CA_ERR_ALIGNMENT;
   return CA_OK;
 }
 
@@ -422,17 +446,9 @@ ca_status ca_dcp_decode(const void* q, const void* k_shards, const void* v_shard
                         int N, int Hq, int Hkv, int64_t Lloc, int D, int dcp, int interleave,
                         const int32_t* seq_lens, float softmax_scale, void* o, float* lse,
                         void* workspace, size_t workspace_bytes, void* stream) {
-  if (!q || !k_shards || !v_shards || !o) return CA_ERR_INVALID_ARG;
-  if (!valid_dtype(dtype) || N <= 0 || Hq <= 0 || Hkv <= 0 || Lloc <= 0 || D <= 0 || dcp <= 0 ||
-      interleave <= 0)
-    return CA_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0 || Lloc % interleave != 0) return CA_ERR_SHAPE;
-  if (dtype != CA_DTYPE_BF16 || D != 128 || Hq / Hkv > 8) return CA_ERR_UNSUPPORTED;
-  if ((int64_t)dcp * N * Hkv * Lloc >= ((int64_t)1 << 31)) return CA_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k_shards) || !aligned16(v_shards) || !aligned16(o) ||
-      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) ||
-      (seq_lens && (reinterpret_cast<uintptr_t>(seq_lens) & 3u)))
-    return CA_ERR_ALIGNMENT;
+  const ca_status chk = check_dcp_decode(q, k_shards, v_shards, dtype, N, Hq, Hkv, Lloc, D, dcp,
+                                         interleave, seq_lens, o, lse);
+  if (chk != CA_OK) return chk;
   const size_t need = ca_dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, dcp, interleave);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return CA_ERR_WORKSPACE;
   DecodeArgs a = decode_args(q, k_shards, v_shards, N, Hq, Hkv, D, dcp, interleave, Lloc, seq_lens,

@@ -35,6 +35,8 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 // Device address of the scratch array for the current device.  In host code
 // the array's name only stands for the host-side shadow symbol, so its device
 // address has to be looked up once per device (with that device current).
+// The cache is per device ordinal: it assumes the device's primary context
+// lives as long as the process (calls after cudaDeviceReset are unsupported).
 void* scratch_address() {
   static std::mutex mu;
   static void* addr[64] = {nullptr};
@@ -43,7 +45,10 @@ void* scratch_address() {
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();  // the failed lookup must not surface in a later, unrelated launch check
+      return nullptr;
+    }
     addr[dev] = p;
   }
   return addr[dev];
@@ -59,18 +64,22 @@ extern "C" ca_status ca_dcp_decode_noalloc(const void* q, const void* k_shards,
                                            int Hkv, int64_t Lloc, int D, int dcp, int interleave,
                                            const int32_t* seq_lens, float softmax_scale, void* o,
                                            float* lse, void* stream) {
-  if (!q || !k_shards || !v_shards || !o) return CA_ERR_INVALID_ARG;
-  if ((dtype != CA_DTYPE_F32 && dtype != CA_DTYPE_BF16) || N <= 0 || Hq <= 0 || Hkv <= 0 ||
-      Lloc <= 0 || D <= 0 || dcp <= 0 || interleave <= 0)
-    return CA_ERR_INVALID_ARG;
-  // the partials must fit in the built-in scratch: reject larger problems
+  // the same argument checks, in the same order, as ca_dcp_decode ...
+  ca_status st = check_dcp_decode(q, k_shards, v_shards, dtype, N, Hq, Hkv, Lloc, D, dcp,
+                                  interleave, seq_lens, o, lse);
+  if (st != CA_OK) return st;
+  // ... then, in place of its workspace check, the partials must fit in the
+  // built-in scratch: larger problems are rejected
   const size_t need = ca_dcp_decode_workspace_size(N, Hq, Hkv, Lloc, D, dcp, interleave);
   if (need == 0 || need > kNoAllocScratchBytes) return CA_ERR_WORKSPACE;
+  // on any other GPU the library's device code (and so the scratch array)
+  // does not exist: say so before looking the array up
+  if ((st = device_is_gb300()) != CA_OK) return st;
   void* scratch = scratch_address();
   if (!scratch) return CA_ERR_CUDA;
-  // ca_dcp_decode validates everything else and runs the decode and merge
-  // kernels on the partials it is given; handing it the scratch array keeps
-  // this call free of any allocation.
+  // ca_dcp_decode runs the decode and merge kernels on the partials it is
+  // given; handing it the scratch array keeps this call free of any
+  // allocation.
   return ca_dcp_decode(q, k_shards, v_shards, dtype, N, Hq, Hkv, Lloc, D, dcp, interleave,
                        seq_lens, softmax_scale, o, lse, scratch, kNoAllocScratchBytes, stream);
 }

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/ctxattn.h"
+
 namespace ca {
 
 // Geometry and options of one ring-attention launch (fused ring or one
@@ -127,5 +129,15 @@ cudaError_t launch_qkv_prologue(const QkvPrologueArgs& a, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// CA_OK when the current device is a GB300 (compute capability 10.3),
+// CA_ERR_UNSUPPORTED for any other device, CA_ERR_CUDA if it cannot be read.
+ca_status device_is_gb300();
+
+// Host checks of a DCP decode call, everything but its workspace (capi.cu).
+ca_status check_dcp_decode(const void* q, const void* k_shards, const void* v_shards,
+                           ca_dtype dtype, int N, int Hq, int Hkv, int64_t Lloc, int D, int dcp,
+                           int interleave, const int32_t* seq_lens, const void* o,
+                           const float* lse);
 
 }  // namespace ca

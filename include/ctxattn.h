@@ -282,14 +282,19 @@ ca_status ca_dcp_decode(const void *q, const void *k_shards,
  * not allocate.  The pages have no counterpart of this call; it exists for
  * such callers only.
  *
- * Same arguments, results and errors as ca_dcp_decode, minus the workspace.
- * The split-KV partials live in a scratch array built into the library's
- * device image: 16 MiB, held on every GPU that loads the library until the
- * process exits.  A problem whose partials need more than that
+ * Same arguments and results as ca_dcp_decode, minus the workspace, and the
+ * same argument checks in the same order (null pointers and sizes, shape,
+ * unsupported dtype or head layout, alignment); where ca_dcp_decode then
+ * checks its workspace, this call checks its scratch.  The split-KV partials
+ * live in a scratch array built into the library's device image: 16 MiB,
+ * held on every GPU that loads the library until the process exits.  A
+ * problem whose partials need more than that
  * (ca_dcp_decode_workspace_size() > 16 MiB) is rejected with
- * CA_ERR_WORKSPACE before anything is enqueued.  The call allocates nothing.
+ * CA_ERR_WORKSPACE before anything is enqueued; on a device other than a
+ * GB300 the call returns CA_ERR_UNSUPPORTED.  The call allocates nothing.
  * The first call on a device looks up the scratch array's device address
- * (cudaGetSymbolAddress, once per device); make that first call before any
+ * (cudaGetSymbolAddress, once per device, cached for the process: calls
+ * after cudaDeviceReset are unsupported); make that first call before any
  * stream capture.  All calls on a device share the one scratch array, so
  * calls whose kernels overlap on the GPU race on it and must be serialised
  * by the caller.  Nothing in it needs to start at zero: every partial the
