@@ -8,7 +8,13 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-FAKE = 4096  # an aligned, never-dereferenced pointer value: validation fails first
+# Base address of a real 1 MiB allocation that these tests pass wherever a
+# call wants a tensor (set by the fixture below; FAKE + 2 and the like stay
+# inside it).  Every call here fails host validation, or is the zero-token
+# cache write that does nothing, so the memory is never read; it is real
+# memory all the same, so that no test hands the library an address nothing
+# owns.
+FAKE = None
 
 
 @pytest.fixture(scope="module")
@@ -17,6 +23,17 @@ def ca():
 
     m.build()
     return m
+
+
+@pytest.fixture(scope="module", autouse=True)
+def real_buffer():
+    from helpers import real_allocation
+
+    global FAKE
+    keep, FAKE = real_allocation(1 << 20)
+    yield
+    FAKE = None
+    del keep
 
 
 def declared_functions():
@@ -270,3 +287,32 @@ def test_missing_library_fails_loudly(ca, monkeypatch):
     monkeypatch.setattr(ca, "_LIB_PATH", "/nonexistent/libctxattn.so")
     with pytest.raises(ca.CtxAttnError):
         ca._load()
+
+
+def test_noalloc_decode_checks_match_the_regular_decode(ca):
+    """The allocation-free decode applies ca_dcp_decode's argument checks
+    first and in the same order, so a problem too large for its 16 MiB
+    scratch still reports whatever else is wrong with it; only a well-formed
+    problem that does not fit gets CA_ERR_WORKSPACE (where the regular call,
+    given room, would go ahead)."""
+    lib = ca._load()
+    S = ca.STATUS
+
+    def both(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=1, N=64, Hq=32, Hkv=8, Lloc=32768, D=128, W=4, I=16, seq=None,
+                 scale=0.0, o=FAKE, lse=FAKE)
+        a.update(kw)
+        args = (a["q"], a["k"], a["v"], a["dtype"], a["N"], a["Hq"], a["Hkv"], a["Lloc"], a["D"], a["W"], a["I"],
+                a["seq"], a["scale"], a["o"], a["lse"])
+        return S[lib.ca_dcp_decode(*args, None, 0, None)], S[lib.ca_dcp_decode_noalloc(*args, None)]
+
+    # partials of 64 sequences x 32 heads over 4 shards of 32768 slots: ~34 MB
+    assert lib.ca_dcp_decode_workspace_size(64, 32, 8, 32768, 128, 4, 16) > (16 << 20)
+    for kw, want in ((dict(q=None), "CA_ERR_INVALID_ARG"), (dict(N=0), "CA_ERR_INVALID_ARG"),
+                     (dict(Hq=30), "CA_ERR_SHAPE"), (dict(Lloc=32760), "CA_ERR_SHAPE"),
+                     (dict(dtype=0), "CA_ERR_UNSUPPORTED"), (dict(D=64), "CA_ERR_UNSUPPORTED"),
+                     (dict(Hq=72, Hkv=8), "CA_ERR_UNSUPPORTED"), (dict(k=FAKE + 8), "CA_ERR_ALIGNMENT"),
+                     (dict(lse=FAKE + 2), "CA_ERR_ALIGNMENT")):
+        assert both(**kw) == (want, want), kw
+    # well formed: the regular call wants its workspace, the other has no room
+    assert both() == ("CA_ERR_WORKSPACE", "CA_ERR_WORKSPACE")

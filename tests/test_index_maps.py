@@ -181,9 +181,12 @@ def test_sequence_divisibility_error(ca):
     rows, _ = read_golden("cp_seq_divisibility.txt")
     S, cp, rem, accepted = rows[0]
     assert S % cp == rem and accepted == 0
+    from helpers import real_allocation
+
     lib = ca._load()
-    fake = 4096  # never dereferenced: validation fails first
-    st = lib.ca_ring_attn_fwd(fake, fake, fake, fake, None, 1, 1, 40, 40, S, 128, cp, 0, 0, 0, 0.0,
+    keep, buf = real_allocation(1 << 16)  # real memory, never read: validation fails first
+    st = lib.ca_ring_attn_fwd(buf, buf, buf, buf, None, 1, 1, 40, 40, S, 128, cp, 0, 0, 0, 0.0,
                               None, 0, None)
     assert ca.STATUS[st] == "CA_ERR_SHAPE"
+    del keep
     del torch
