@@ -19,9 +19,12 @@
 // with P moved from the accumulator layout to the operand layout by
 // movmatrix.  Row maxima use a lazy rescale: the reference moves only when a
 // 16-token group's maximum passes it by more than 8 (log2); the rescale of
-// the register-resident O is cheap here.  At the end of an item the four
-// warps' partial states are LSE-merged in shared memory and one partial
-// (o, lse) per query head is written.
+// the register-resident O is cheap here.  Each head keeps two row sums: of p
+// as computed (for the log-sum-exp) and of p rounded to bf16 as the PV MMA
+// consumes it (O is divided by this one, so the weights in O and in its
+// normaliser are the same and o is a convex combination of V rows).  At the
+// end of an item the four warps' partial states are LSE-merged in shared
+// memory and one partial (o, lse) per query head is written.
 #include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -49,8 +52,8 @@ constexpr int kMaxG = 8;
 
 constexpr uint32_t kSmemStages = 0;
 constexpr uint32_t kSmemMergeO = kStages * kStageBytes;                    // [warps][8][128] f32
-constexpr uint32_t kSmemMergeML = kSmemMergeO + kConsumerWarps * kMaxG * kD * 4;  // [warps][8] m, l
-constexpr uint32_t kSmemBar = kSmemMergeML + kConsumerWarps * kMaxG * 2 * 4;
+constexpr uint32_t kSmemMergeML = kSmemMergeO + kConsumerWarps * kMaxG * kD * 4;  // [warps][8] m, l, lr
+constexpr uint32_t kSmemBar = kSmemMergeML + kConsumerWarps * kMaxG * 3 * 4;
 constexpr uint32_t kSmemAbort = kSmemBar + (2 * kStages + 1) * 8;
 constexpr uint32_t kSmemUsed = kSmemAbort + 4;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
@@ -256,7 +259,7 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
           qf[kk][1] = g < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * t) : 0u;
         }
       }
-      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, lr0 = 0.f, lr1 = 0.f;
       float acc[kD / 16][4];
 #pragma unroll
       for (int mb = 0; mb < kD / 16; ++mb) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.f;
@@ -314,6 +317,7 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
           if (mx0 > m0 + 8.f || (m0 == -INFINITY && mx0 != -INFINITY)) {
             const float f = m0 == -INFINITY ? 0.f : ex2(m0 - mx0);
             l0 *= f;
+            lr0 *= f;
 #pragma unroll
             for (int mb = 0; mb < kD / 16; ++mb) {
               acc[mb][0] *= f;
@@ -324,6 +328,7 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
           if (mx1 > m1 + 8.f || (m1 == -INFINITY && mx1 != -INFINITY)) {
             const float f = m1 == -INFINITY ? 0.f : ex2(m1 - mx1);
             l1 *= f;
+            lr1 *= f;
 #pragma unroll
             for (int mb = 0; mb < kD / 16; ++mb) {
               acc[mb][1] *= f;
@@ -334,10 +339,13 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
           const float r0 = m0 == -INFINITY ? 0.f : m0;
           const float r1 = m1 == -INFINITY ? 0.f : m1;
           const float p0 = ex2(x0 - r0), p1 = ex2(x1 - r1), p2 = ex2(x2 - r0), p3 = ex2(x3 - r1);
+          const uint32_t w01 = pack_bf16x2(p0, p1), w23 = pack_bf16x2(p2, p3);
           l0 += p0 + p2;
           l1 += p1 + p3;
-          const uint32_t pb0 = movm_t(pack_bf16x2(p0, p1));
-          const uint32_t pb1 = movm_t(pack_bf16x2(p2, p3));
+          lr0 += __uint_as_float(w01 << 16) + __uint_as_float(w23 << 16);
+          lr1 += __uint_as_float(w01 & 0xFFFF0000u) + __uint_as_float(w23 & 0xFFFF0000u);
+          const uint32_t pb0 = movm_t(w01);
+          const uint32_t pb1 = movm_t(w23);
 #pragma unroll
           for (int mb = 0; mb < kD / 16; ++mb) {
             const int q4 = lane >> 3;
@@ -361,14 +369,18 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       for (int o = 4; o < 32; o <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, o);
         l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+        lr0 += __shfl_xor_sync(0xffffffffu, lr0, o);
+        lr1 += __shfl_xor_sync(0xffffffffu, lr1, o);
       }
       float* mow = mo + warp * kMaxG * kD;
-      float* mlw = mml + warp * kMaxG * 2;
+      float* mlw = mml + warp * kMaxG * 3;
       if (lane < 4) {
-        mlw[2 * (2 * t) + 0] = m0;
-        mlw[2 * (2 * t) + 1] = l0;
-        mlw[2 * (2 * t + 1) + 0] = m1;
-        mlw[2 * (2 * t + 1) + 1] = l1;
+        mlw[3 * (2 * t) + 0] = m0;
+        mlw[3 * (2 * t) + 1] = l0;
+        mlw[3 * (2 * t) + 2] = lr0;
+        mlw[3 * (2 * t + 1) + 0] = m1;
+        mlw[3 * (2 * t + 1) + 1] = l1;
+        mlw[3 * (2 * t + 1) + 2] = lr1;
       }
 #pragma unroll
       for (int mb = 0; mb < kD / 16; ++mb) {
@@ -386,19 +398,20 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       for (int idx = threadIdx.x; idx < G * kD; idx += kConsumerWarps * 32) {
         const int h = idx / kD, d = idx % kD;
         float M = -INFINITY;
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[w * kMaxG * 2 + 2 * h]);
-        float L = 0.f, O = 0.f;
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[w * kMaxG * 3 + 3 * h]);
+        float L = 0.f, Lr = 0.f, O = 0.f;
         if (M != -INFINITY) {
           for (int w = 0; w < kConsumerWarps; ++w) {
-            const float mw = mml[w * kMaxG * 2 + 2 * h];
+            const float mw = mml[w * kMaxG * 3 + 3 * h];
             if (mw == -INFINITY) continue;
             const float f = ex2(mw - M);
-            L += mml[w * kMaxG * 2 + 2 * h + 1] * f;
+            L += mml[w * kMaxG * 3 + 3 * h + 1] * f;
+            Lr += mml[w * kMaxG * 3 + 3 * h + 2] * f;
             O += mo[(w * kMaxG + h) * kD + d] * f;
           }
         }
         const int64_t prow = (int64_t)pidx * R + orow0 + h;
-        a.o_parts[prow * kD + d] = L > 0.f ? O / L : 0.f;
+        a.o_parts[prow * kD + d] = L > 0.f ? O / Lr : 0.f;
         if (d == 0) a.lse_parts[prow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
       }
       // every warp has read the shared partials before the next item rewrites them

@@ -33,6 +33,7 @@
 // so P may grow far above 1 meanwhile.  Const max never rescales: merging the
 // ring steps is pure addition.
 #include <atomic>
+#include <type_traits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -453,12 +454,50 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
+// The two row sums of a softmax row.  `l` sums p as computed (fp32): it gives
+// the log-sum-exp.  `lr` is the sum O is divided by.  On a tile that needs a
+// mask (a causal diagonal, a shard's ragged end) lr sums p as the PV product
+// consumes it, rounded to bf16, so that every weight in the numerator is
+// matched by the same weight in the denominator ("Accumulate, then normalize
+// once": the accumulator and its row sum come from one set of weights): the
+// rows that see only a handful of keys -- where one weight's rounding error
+// would otherwise move o by up to 2^-8 |o| -- get o as an exact convex
+// combination of their V rows up to fp32 accumulation.  On unmasked tiles lr
+// takes the fp32 p like l: there a row's weight is spread over whole tiles
+// of keys, and forming the rounded sum on every tile costs 8-14 % of the
+// kernel's throughput (the softmax warps' issue slots are the bound).
+// masked tiles: classify each 32-column chunk across the warp (variant knob)
+constexpr bool kChunkClassify = true;
+
+struct RowSums {
+  uint64_t l2, lr2;  // packed pairs of partial sums
+};
+
+// Adds the two bf16 halves of w, widened exactly, into the pair sum lr2.
+__device__ __forceinline__ void add_bf16_pair(uint64_t& lr2, uint32_t w) {
+  lr2 = f2_add(lr2, f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)));
+}
+
+// p for one pair of scores: sums it into `rs` (lr too when kInl) and returns
+// it as a packed bf16 pair (lo = p0).
+template <bool kInl>
+__device__ __forceinline__ uint32_t exp_pair(float s0, float s1, uint64_t sl2_2, uint64_t nref_2,
+                                             RowSums& rs) {
+  float a0, a1;
+  f2_unpack(f2_fma(f2_pack(s0, s1), sl2_2, nref_2), a0, a1);
+  const float p0 = ex2(a0), p1 = ex2(a1);
+  const uint32_t w = pack_bf16x2(p0, p1);
+  rs.l2 = f2_add(rs.l2, f2_pack(p0, p1));
+  if (kInl) add_bf16_pair(rs.lr2, w);
+  return w;
+}
+
 // 32 scores -> 16 packed bf16 pairs of p = 2^(s*sl2 - ref), written to TMEM
-// columns [16*ch, 16*ch + 16) of the row; adds the chunk's p into `sum2`
-// (two partial sums, one per element of each pair).
-template <bool kMask>
+// columns [16*ch, 16*ch + 16) of the row and kept in pk; adds the chunk's p
+// into `rs`.
+template <bool kMask, bool kInl>
 __device__ __forceinline__ void exp_chunk(const uint32_t (&r)[32], int ch, int vis_max,
-                                          uint64_t sl2_2, uint64_t nref_2, uint64_t& sum2,
+                                          uint64_t sl2_2, uint64_t nref_2, RowSums& rs,
                                           uint32_t tS) {
   uint32_t pk[16];
 #pragma unroll
@@ -468,39 +507,58 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&r)[32], int ch, int v
       if (ch * 32 + 2 * x > vis_max) s0 = -INFINITY;
       if (ch * 32 + 2 * x + 1 > vis_max) s1 = -INFINITY;
     }
-    float a0, a1;
-    f2_unpack(f2_fma(f2_pack(s0, s1), sl2_2, nref_2), a0, a1);
-    const float p0 = ex2(a0), p1 = ex2(a1);
-    sum2 = f2_add(sum2, f2_pack(p0, p1));
-    pk[x] = pack_bf16x2(p0, p1);
+    pk[x] = exp_pair<kInl>(s0, s1, sl2_2, nref_2, rs);
   }
   tmem_st16(tS + ch * 16, pk);
 }
 
+// A tile's (l, lr): on an unmasked tile lr is l itself.
+template <bool kMask>
+__device__ __forceinline__ float2 tile_sums(const RowSums& rs) {
+  float lo, hi;
+  f2_unpack(rs.l2, lo, hi);
+  const float l = lo + hi;
+  if (!kMask) return make_float2(l, l);
+  f2_unpack(rs.lr2, lo, hi);
+  return make_float2(l, lo + hi);
+}
+
 // Online max, speculative single pass over one S row: p = 2^(s*sl2 - m)
 // against the row's current reference m, packed into registers (pk) and
-// summed into sum2, while the row maximum of the raw scores is tracked.
+// summed into rs, while the row maximum of the raw scores is tracked.
 // Nothing is written to TMEM, so if the maximum turns out to lie more than
 // 64 (log2) above the reference the caller still has S to start over from.
 template <bool kMask>
 __device__ __forceinline__ float spec_row(uint32_t tS, int vis_max, uint64_t sl2_2, uint64_t nref_2,
-                                          uint32_t (&pk)[64], uint64_t& sum2) {
+                                          uint32_t (&pk)[64], RowSums& rs) {
+  constexpr bool kInl = kMask;  // masked tiles form the rounded sum
   uint32_t ra[32], rb[32];
   float mx = -INFINITY;
-  auto chunk = [&](const uint32_t(&r)[32], int ch) {
-    mx = chunk_max<kMask>(r, ch * 32, vis_max, mx);
+  // one chunk, masked element by element or not at all (kM)
+  auto chunk_as = [&](const uint32_t(&r)[32], int ch, auto kM) {
+    constexpr bool m = decltype(kM)::value;
+    mx = chunk_max<m>(r, ch * 32, vis_max, mx);
 #pragma unroll
     for (int x = 0; x < 16; ++x) {
       float s0 = __uint_as_float(r[2 * x]), s1 = __uint_as_float(r[2 * x + 1]);
-      if (kMask) {
+      if (m) {
         if (ch * 32 + 2 * x > vis_max) s0 = -INFINITY;
         if (ch * 32 + 2 * x + 1 > vis_max) s1 = -INFINITY;
       }
-      float a0, a1;
-      f2_unpack(f2_fma(f2_pack(s0, s1), sl2_2, nref_2), a0, a1);
-      const float p0 = ex2(a0), p1 = ex2(a1);
-      sum2 = f2_add(sum2, f2_pack(p0, p1));
-      pk[16 * ch + x] = pack_bf16x2(p0, p1);
+      pk[16 * ch + x] = exp_pair<kInl>(s0, s1, sl2_2, nref_2, rs);
+    }
+  };
+  // a masked tile's chunks classified across the warp as in exp_chunk_masked
+  auto chunk = [&](const uint32_t(&r)[32], int ch) {
+    if (!kMask) {
+      chunk_as(r, ch, std::false_type{});
+    } else if (kChunkClassify && __all_sync(0xffffffffu, ch * 32 + 31 <= vis_max)) {
+      chunk_as(r, ch, std::false_type{});
+    } else if (kChunkClassify && __all_sync(0xffffffffu, ch * 32 > vis_max)) {
+#pragma unroll
+      for (int x = 0; x < 16; ++x) pk[16 * ch + x] = 0u;
+    } else {
+      chunk_as(r, ch, std::true_type{});
     }
   };
   tmem_ld32(tS, ra);
@@ -522,33 +580,67 @@ __device__ __forceinline__ float spec_row(uint32_t tS, int vis_max, uint64_t sl2
   return mx;
 }
 
-// Pass 2 over one S row: exp, row sum, P (bf16) back into TMEM, with the
+// Pass 2 over one S row: exp, row sums, P (bf16) back into TMEM and kept in
+// pk, with the next 32-column load in flight while the current chunk is
+// processed.  P block ch overwrites S columns [16ch, 16ch+16), which were
+// already read.  Returns the tile's (l, lr) sums (lr only when kInl).
+// A chunk of a masked tile, classified across the warp: where every row of
+// the warp sees all 32 columns the unmasked code runs, where none sees any
+// the chunk's P is zero (no exp, nothing summed), and only a chunk that the
+// warp's visibility limits cross is masked element by element.  On a
+// diagonal tile the limits of a warp's 32 consecutive rows span 32
+// consecutive columns, so at most two of a row's four chunks are masked.
+template <bool kInl>
+__device__ __forceinline__ void exp_chunk_masked(const uint32_t (&r)[32], int ch, int vis_max,
+                                                 uint64_t sl2_2, uint64_t nref_2, RowSums& rs,
+                                                 uint32_t tS) {
+  if (kChunkClassify && __all_sync(0xffffffffu, ch * 32 + 31 <= vis_max)) {
+    exp_chunk<false, kInl>(r, ch, vis_max, sl2_2, nref_2, rs, tS);
+  } else if (kChunkClassify && __all_sync(0xffffffffu, ch * 32 > vis_max)) {
+    const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    tmem_st16(tS + ch * 16, z);
+  } else {
+    exp_chunk<true, kInl>(r, ch, vis_max, sl2_2, nref_2, rs, tS);
+  }
+}
+
+// The chunk of a masked tile (kMask) or of an unmasked one.
+template <bool kMask>
+__device__ __forceinline__ void exp_chunk_any(const uint32_t (&r)[32], int ch, int vis_max,
+                                              uint64_t sl2_2, uint64_t nref_2, RowSums& rs,
+                                              uint32_t tS) {
+  if (kMask)
+    exp_chunk_masked<true>(r, ch, vis_max, sl2_2, nref_2, rs, tS);
+  else
+    exp_chunk<false, false>(r, ch, vis_max, sl2_2, nref_2, rs, tS);
+}
+
+// Pass 2 over one S row: exp, row sums, P (bf16) back into TMEM, with the
 // next 32-column load in flight while the current chunk is processed.  P
 // block ch overwrites S columns [16ch, 16ch+16), which were already read.
+// Returns the tile's (l, lr) sums.
 template <bool kMask>
-__device__ __forceinline__ float exp_row_to_tmem(uint32_t tS, int vis_max, float sl2, float ref) {
+__device__ __forceinline__ float2 exp_row_to_tmem(uint32_t tS, int vis_max, float sl2, float ref) {
   uint32_t ra[32], rb[32];
   const uint64_t sl2_2 = f2_pack(sl2, sl2), nref_2 = f2_pack(-ref, -ref);
-  uint64_t sum2 = f2_pack(0.f, 0.f);
+  RowSums rs{f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
   tmem_ld32(tS, ra);
   tmem_ld_wait();
   reg_fence(ra);
   tmem_ld32(tS + 32, rb);
-  exp_chunk<kMask>(ra, 0, vis_max, sl2_2, nref_2, sum2, tS);
+  exp_chunk_any<kMask>(ra, 0, vis_max, sl2_2, nref_2, rs, tS);
   tmem_ld_wait();
   reg_fence(rb);
   tmem_ld32(tS + 64, ra);
-  exp_chunk<kMask>(rb, 1, vis_max, sl2_2, nref_2, sum2, tS);
+  exp_chunk_any<kMask>(rb, 1, vis_max, sl2_2, nref_2, rs, tS);
   tmem_ld_wait();
   reg_fence(ra);
   tmem_ld32(tS + 96, rb);
-  exp_chunk<kMask>(ra, 2, vis_max, sl2_2, nref_2, sum2, tS);
+  exp_chunk_any<kMask>(ra, 2, vis_max, sl2_2, nref_2, rs, tS);
   tmem_ld_wait();
   reg_fence(rb);
-  exp_chunk<kMask>(rb, 3, vis_max, sl2_2, nref_2, sum2, tS);
-  float lo, hi;
-  f2_unpack(sum2, lo, hi);
-  return lo + hi;
+  exp_chunk_any<kMask>(rb, 3, vis_max, sl2_2, nref_2, rs, tS);
+  return tile_sums<kMask>(rs);
 }
 
 // O *= f for this thread's row, out of line: the deferred reference move of
@@ -846,7 +938,8 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
       const float c_log2 = c_nat * kLog2e;
       float m = -INFINITY;  // reference max, log2 units (online mode)
       int pend = 0;         // reference move (log2 units) due before the next tile
-      float l = 0.f;
+      float l = 0.f;   // row sum of p as computed (log-sum-exp)
+      float lr = 0.f;  // row sum of p rounded to bf16 (normalisation)
       TileIter it;
       it.begin(P, U);
       int64_t row_lim = 0;
@@ -881,13 +974,15 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
           tmem_st_wait();
         };
         float mref;
-        bool p_done = false;  // P already in TMEM and its sum in l
+        bool p_done = false;  // P already in TMEM and its sums in tl, tlr
+        float tl = 0.f, tlr = 0.f;  // the tile's l and lr
         if (!const_max && __any_sync(0xffffffffu, pend > 0)) {
           // the reference move left by the previous tile (whose PV has
           // completed: it precedes this tile's S in the MMA order)
           const float fac = pend > 0 ? __int_as_float((127 - pend) << 23) : 1.f;
           rescale_o_row(tO, fac);
           l *= fac;
+          lr *= fac;
           m += (float)pend;
           pend = 0;
         }
@@ -896,11 +991,11 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         } else if (j > 0 && !__any_sync(0xffffffffu, m == -INFINITY)) {
           // within a unit the row maximum rarely moves past the lazy-rescale
           // threshold: try the single pass against the current reference
-          uint32_t pk[64];
           const uint64_t sl2_2 = f2_pack(P.scale_log2, P.scale_log2), nref_2 = f2_pack(-m, -m);
-          uint64_t sum2 = f2_pack(0.f, 0.f);
-          const float mx = need_mask ? spec_row<true>(tS, vis_max, sl2_2, nref_2, pk, sum2)
-                                     : spec_row<false>(tS, vis_max, sl2_2, nref_2, pk, sum2);
+          RowSums rs{f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+          uint32_t pk[64];
+          const float mx = need_mask ? spec_row<true>(tS, vis_max, sl2_2, nref_2, pk, rs)
+                                     : spec_row<false>(tS, vis_max, sl2_2, nref_2, pk, rs);
           // how far the tile's maximum lies above the reference.  Up to 64
           // (log2) this tile's P, l and O stay far from fp32 overflow against
           // the old reference, so P is kept; past the lazy-rescale threshold
@@ -909,10 +1004,10 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
           const float jump = mx * P.scale_log2 - m;
           if (__all_sync(0xffffffffu, !(jump > 64.f))) {
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) tmem_st16(tS + ch * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * ch]));
-            float lo, hi;
-            f2_unpack(sum2, lo, hi);
-            l += lo + hi;
+            for (int ch = 0; ch < 4; ++ch) tmem_st16(tS + ch * 16, &pk[16 * ch]);
+            const float2 t = need_mask ? tile_sums<true>(rs) : tile_sums<false>(rs);
+            tl = t.x;
+            tlr = t.y;
             if (jump > kRescaleThreshold) pend = (int)ceilf(jump);  // 49 .. 64
             p_done = true;
           }
@@ -929,6 +1024,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
             fac = (m == -INFINITY) ? 0.f : ex2(m - mx);
             need_o = (m != -INFINITY) && (j > 0);
             l *= fac;
+            lr *= fac;
             m = mx;
           }
           if (__any_sync(0xffffffffu, need_o)) rescale_o(need_o ? fac : 1.f);
@@ -937,10 +1033,13 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         // pass 2: p = 2^(s*scale*log2e - ref), row sum, bf16 P written over
         // the S columns already consumed (P column block ch < S block ch+1)
         if (!p_done) {
-          const float psum = need_mask ? exp_row_to_tmem<true>(tS, vis_max, P.scale_log2, mref)
-                                       : exp_row_to_tmem<false>(tS, vis_max, P.scale_log2, mref);
-          l += psum;
+          const float2 t = need_mask ? exp_row_to_tmem<true>(tS, vis_max, P.scale_log2, mref)
+                                     : exp_row_to_tmem<false>(tS, vis_max, P.scale_log2, mref);
+          tl = t.x;
+          tlr = t.y;
         }
+        l += tl;
+        lr += tlr;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(kBarPFull + i));
@@ -952,12 +1051,17 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
       tc_fence_after();
       if (releaser) mbar_arrive(bar(kBarKvEmpty + (int)((kvpos + 2 * (uint64_t)n - 1) % kNSlot)));  // V_(n-1)
       kvpos += 2 * (uint64_t)n;
+      // O is divided by the sum of the weights it was accumulated with (lr);
+      // the log-sum-exp comes from the unrounded sum l.  An unnormalised
+      // const-max partial carries O * l / lr, so that the merge, which
+      // divides by the steps' summed l, still gives each step's O / lr its
+      // weight l.
       float inv, lse;
       if (const_max) {
-        inv = P.a.unnormalized ? 1.f : 1.f / fmaxf(l, 1e-37f);
+        inv = P.a.unnormalized ? (lr > 0.f ? l / lr : 1.f) : 1.f / fmaxf(lr, 1e-37f);
         lse = c_nat + logf(l);
       } else if (l > 0.f) {
-        inv = 1.f / l;
+        inv = 1.f / lr;
         lse = (m + log2f(l)) * kLn2;
       } else {
         inv = 0.f;

@@ -16,6 +16,46 @@ def np32(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy()
 
 
+def real_allocation(nbytes: int):
+    """A real buffer of nbytes for calls whose pointers must not be read:
+    device memory when a GPU is present, else host memory.  Returns (owner,
+    256-byte aligned base address); keep the owner alive while the address
+    is in use."""
+    if torch.cuda.is_available():
+        buf = torch.empty(nbytes + 256, dtype=torch.uint8, device="cuda")
+    else:
+        buf = torch.empty(nbytes + 256, dtype=torch.uint8)
+    base = buf.data_ptr()
+    return buf, (base + 255) & ~255
+
+
+def bf16_rounding(x) -> np.ndarray:
+    """|bf16(x) - x| elementwise (round to nearest even): what storing the
+    exact value x as a bf16 output costs by itself."""
+    x = np.asarray(x, dtype=np.float64)
+    r = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    return np.abs(r - x)
+
+
+def bf16_bound(o, ro, what=""):
+    """Per element, the fixed bf16 bound 2e-2 plus the one error no kernel can
+    avoid with a bf16 output: the exact value's own rounding to bf16, at most
+    half a bf16 ulp (random draws reach |o| above 4, where that half ulp
+    alone is 1.6e-2).  Nothing else is allowed for: the P weights the PV
+    product uses are matched by the same weights in the row sum that
+    normalises it, so their rounding does not show up as an error
+    proportional to |v|.  Returns the largest error."""
+    g = np.asarray(o, dtype=np.float64)
+    ro = np.asarray(ro, dtype=np.float64).reshape(g.shape)
+    bound = BF16_MAX_ABS + bf16_rounding(ro)
+    err = np.abs(g - ro)
+    worst = np.unravel_index(int(np.argmax(err - bound)), err.shape)
+    assert np.isfinite(g).all(), what
+    assert (err <= bound).all(), (f"{what}: err {err[worst]:.3e} > bound {bound[worst]:.3e} "
+                                  f"(|o| {abs(ro[worst]):.3f})")
+    return float(err.max())
+
+
 def assert_close(gpu_o, ref_o, gpu_lse=None, ref_lse=None, dtype=torch.bfloat16, what=""):
     g = np.asarray(gpu_o, dtype=np.float64).reshape(np.asarray(ref_o).shape)
     err = np.abs(g - ref_o)

@@ -101,3 +101,26 @@ def test_decode_matches_global_attention(ca):
                                   rows=[h * Ln for h in range(Hq)])
         assert_close(np32(o[n]), ro, np32(lse[n]), rl, what=f"decode vs global n={n}")
     del synth
+
+
+@pytest.mark.parametrize("scale", [None, 0.5])
+def test_decode_constant_v_gives_v_exactly(ca, scale):
+    """When every cached token of a KV head holds the same value row, each
+    query head's output is that row.  Every split divides its O by the sum
+    of the bf16 weights its MMA used, and the LSE merge's weights sum to one
+    up to fp32 rounding, so the bf16 output rounds back to V exactly; scale
+    0.5 lets a few keys dominate each head, and one sequence holds a single
+    token.  Values up to 16 in size."""
+    from context_attention_gb300 import synth
+
+    N, Hq, Hkv, W, I, Lloc = 3, 16, 2, 4, 16, 1024
+    q, k, _ = synth.decode_inputs(N, Hq, Hkv, 128, W, Lloc, 41, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(42)
+    row = ((torch.rand(N, Hkv, 128, generator=g, device="cuda") * 2 - 1) * 16).to(torch.bfloat16)
+    v = row[None, :, :, None, :].expand(W, N, Hkv, Lloc, 128).contiguous()
+    sl = torch.tensor([W * Lloc, 1, 777], dtype=torch.int32, device="cuda")
+    o, lse = ca.dcp_decode(q, k, v, I, seq_lens=sl, softmax_scale=scale)
+    want = row.repeat_interleave(Hq // Hkv, dim=1)
+    bad = (o != want).sum().item()
+    assert bad == 0, f"{bad} elements differ from V; worst {(o.float() - want.float()).abs().max().item():.3e}"

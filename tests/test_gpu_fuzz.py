@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import assert_close, np32
+from helpers import assert_close, bf16_bound, np32
 
 pytestmark = pytest.mark.gpu
 
@@ -55,32 +55,11 @@ def test_ring_random_shapes(ca, c):
     if c["dtype"] == torch.float32:
         assert_close(np32(o), ro, np32(lse), rl, dtype=c["dtype"], what=str(c))
         return
-    bf16_bound(np32(o), ro, np32(v), c["G"], what=str(c))
+    bf16_bound(np32(o), ro, what=str(c))
     # lse and the mean error keep the fixed bounds
     g, r = np32(lse).astype(np.float64).reshape(-1), np.asarray(rl).reshape(-1)
     assert np.abs(g - r).max() <= 1e-3, str(c)
     assert np.abs(np32(o).astype(np.float64).reshape(ro.shape) - ro).mean() <= 2e-3, str(c)
-
-
-def bf16_bound(o, ro, v, G, what):
-    """Random draws reach rows the configured workloads do not (any softmax
-    scale; causal rows with a handful of keys and large values), where the
-    bf16 arithmetic alone can pass the fixed 2e-2.  Per element they are held
-    to what that arithmetic gives: half a bf16 ulp of the exact output (with
-    room for fp32 accumulation, 2^-8 |o|), plus the bf16 rounding of P, whose
-    relative error 2^-9 per weight (and the row sum taken before rounding)
-    moves o by at most 2^-8 of the head's largest |v|, plus 1e-3.  A wrong
-    mask, shard or scale moves o by the size of v itself."""
-    g = np.asarray(o, dtype=np.float64)                    # [B, Hq, S, D]
-    ro = np.asarray(ro, dtype=np.float64).reshape(g.shape)
-    vmax = np.abs(v).max(axis=(2, 3))                      # [B, Hkv]
-    vmax_q = np.repeat(vmax, G, axis=1)[:, :, None, None]  # per query head
-    bound = 2.0 ** -8 * np.abs(ro) + 2.0 ** -8 * vmax_q + 1e-3
-    err = np.abs(g - ro)
-    worst = np.unravel_index(int(np.argmax(err - bound)), err.shape)
-    assert np.isfinite(g).all(), what
-    assert (err <= bound).all(), (f"{what}: err {err[worst]:.3e} > bound {bound[worst]:.3e} "
-                                  f"(|o| {abs(ro[worst]):.3f})")
 
 
 def decode_draws(n, seed):

@@ -77,6 +77,36 @@ def test_fp32_odd_head_dims(ca, mode, D):
 
 @pytest.mark.parametrize("mode", ["online_max", "const_max"])
 @pytest.mark.parametrize("causal,layout", [(False, "contiguous"), (True, "contiguous"), (True, "striped")])
+@pytest.mark.parametrize("wide", [False, True])
+def test_bf16_constant_v_gives_v_exactly(ca, mode, causal, layout, wide):
+    """Invariant (d) on the GPU: when every key of a head carries the same
+    value row, the output is that row, whatever the weights.  The weights
+    the PV product uses are bf16; on a tile that needs a mask (a causal
+    diagonal, a shard's ragged end) O is divided by the sum of those same
+    rounded weights, so o = V up to fp32 accumulation, which the bf16 output
+    rounds back to V itself.  With 96-key shards every tile is ragged, so
+    every row is normalised that way.  Causal rows near a shard's start see
+    a handful of keys, and a wide score spread (scale 0.5; 0.25 in const
+    max, whose bound must stay within ~85 nats of a row's lone key) lets one
+    key dominate: the cases in which dividing by the unrounded weights' sum
+    would be off by up to 2^-8 |V|.  Values up to 16 in size."""
+    B, Hq, Hkv, S, D, cp = 1, 4, 2, 384, 128, 4
+    scale = {"online_max": 0.5, "const_max": 0.25}[mode] if wide else None
+    q, k, _ = gen(B, Hq, Hkv, S, D, 32, torch.bfloat16)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(33)
+    row = ((torch.rand(B, Hkv, 1, D, generator=g, device="cuda") * 2 - 1) * 16).to(torch.bfloat16)
+    v = row.expand(B, Hkv, S, D).contiguous()
+    o, lse = ca.ring_attn_fwd(q, k, v, cp, mode=mode, causal=causal, layout=layout, softmax_scale=scale)
+    want = row.repeat_interleave(Hq // Hkv, dim=1).expand(B, Hq, S, D)
+    bad = (o != want).sum().item()
+    assert bad == 0, f"{bad} elements differ from V; worst {(o.float() - want.float()).abs().max().item():.3e}"
+    ro, rl = oracle_ring(q, k, v, cp, mode, causal, layout, scale=scale)
+    assert np.abs(np32(lse).astype(np.float64).reshape(-1) - np.asarray(rl).reshape(-1)).max() <= 1e-3
+
+
+@pytest.mark.parametrize("mode", ["online_max", "const_max"])
+@pytest.mark.parametrize("causal,layout", [(False, "contiguous"), (True, "contiguous"), (True, "striped")])
 def test_bf16_small(ca, mode, causal, layout):
     """bf16, D=128, B=1, H=2, S=1024, cp=4 (Ls=256: two query tiles per unit)."""
     q, k, v = gen(1, 2, 2, 1024, 128, 3, torch.bfloat16)
