@@ -388,9 +388,8 @@ ca_status ca_qkv_prologue(const void* x_q, const void* x_k, const void* x_v, con
 // ------------------------------------------------------------------ decode
 size_t ca_dcp_decode_workspace_size(int N, int Hq, int Hkv, int64_t Lloc, int D, int dcp,
                                     int interleave) {
-  (void)Hkv;
   (void)interleave;
-  if (N <= 0 || Hq <= 0 || Lloc <= 0 || D <= 0 || dcp <= 0) return 0;
+  if (N <= 0 || Hq <= 0 || Hkv <= 0 || Lloc <= 0 || D <= 0 || dcp <= 0) return 0;
   int64_t chunk;
   int splits;
   dcp_decode_split(Lloc, &chunk, &splits);
@@ -457,8 +456,7 @@ ca_status ca_dcp_decode(const void* q, const void* k_shards, const void* v_shard
 }
 
 size_t ca_ring_decode_workspace_size(int B, int Hq, int Hkv, int64_t S, int D, int cp_size) {
-  (void)Hkv;
-  if (B <= 0 || Hq <= 0 || S <= 0 || D <= 0 || cp_size <= 0 || S % cp_size != 0) return 0;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || cp_size <= 0 || S % cp_size != 0) return 0;
   int64_t chunk;
   int splits;
   dcp_decode_split(S / cp_size, &chunk, &splits);

@@ -59,4 +59,24 @@ inline bool encode_bf16_3d_sw128(CUtensorMap* map, const void* base, uint64_t de
   return r == CUDA_SUCCESS;
 }
 
+// bf16 tensor map over a row-major [rows, 128] matrix seen as three
+// dimensions -- 64 columns, rows, and the two 64-column halves of a row -- so
+// that one box of [2, box_rows, 64] brings both halves of box_rows rows,
+// stored half after half: [half][row][64], each 128-byte row swizzled as
+// in a [box_rows, 64] box.  Rows >= `rows` read as zero.
+inline bool encode_bf16_halves_sw128(CUtensorMap* map, const void* base, uint64_t rows,
+                                     uint32_t box_rows) {
+  auto fn = get_encode_tiled();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, rows, 2};
+  cuuint64_t strides[2] = {256, 128};
+  cuuint32_t box[3] = {64, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace ca
