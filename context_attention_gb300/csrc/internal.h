@@ -64,6 +64,11 @@ cudaError_t launch_const_max_bound(const void* q, const void* k, int is_bf16, in
                                    int Hq, int Hkv, int64_t S, int D, float scale,
                                    float* c, float* kmax2, cudaStream_t stream);
 
+// The LSE merge kernels wait on the grid dependency before they read a
+// partial and are launched with programmatic stream serialization, so the
+// kernel ahead of them (the decode partials, which release them early) and
+// the merge overlap their launch; after any other kernel the wait is the
+// ordinary stream order.
 cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int n,
                              int64_t R, int D, const float* c, void* o, int out_bf16,
                              float* lse, cudaStream_t stream);
