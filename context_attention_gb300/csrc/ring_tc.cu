@@ -466,8 +466,6 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 // takes the fp32 p like l: there a row's weight is spread over whole tiles
 // of keys, and forming the rounded sum on every tile costs 8-14 % of the
 // kernel's throughput (the softmax warps' issue slots are the bound).
-// masked tiles: classify each 32-column chunk across the warp (variant knob)
-constexpr bool kChunkClassify = true;
 
 struct RowSums {
   uint64_t l2, lr2;  // packed pairs of partial sums
@@ -552,9 +550,9 @@ __device__ __forceinline__ float spec_row(uint32_t tS, int vis_max, uint64_t sl2
   auto chunk = [&](const uint32_t(&r)[32], int ch) {
     if (!kMask) {
       chunk_as(r, ch, std::false_type{});
-    } else if (kChunkClassify && __all_sync(0xffffffffu, ch * 32 + 31 <= vis_max)) {
+    } else if (__all_sync(0xffffffffu, ch * 32 + 31 <= vis_max)) {
       chunk_as(r, ch, std::false_type{});
-    } else if (kChunkClassify && __all_sync(0xffffffffu, ch * 32 > vis_max)) {
+    } else if (__all_sync(0xffffffffu, ch * 32 > vis_max)) {
 #pragma unroll
       for (int x = 0; x < 16; ++x) pk[16 * ch + x] = 0u;
     } else {
@@ -594,9 +592,9 @@ template <bool kInl>
 __device__ __forceinline__ void exp_chunk_masked(const uint32_t (&r)[32], int ch, int vis_max,
                                                  uint64_t sl2_2, uint64_t nref_2, RowSums& rs,
                                                  uint32_t tS) {
-  if (kChunkClassify && __all_sync(0xffffffffu, ch * 32 + 31 <= vis_max)) {
+  if (__all_sync(0xffffffffu, ch * 32 + 31 <= vis_max)) {
     exp_chunk<false, kInl>(r, ch, vis_max, sl2_2, nref_2, rs, tS);
-  } else if (kChunkClassify && __all_sync(0xffffffffu, ch * 32 > vis_max)) {
+  } else if (__all_sync(0xffffffffu, ch * 32 > vis_max)) {
     const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     tmem_st16(tS + ch * 16, z);
   } else {

@@ -90,9 +90,12 @@ def parity_report(what, gpu_o, ref_o, gpu_lse, ref_lse, oracle_s):
     # half a bf16 ulp of the exact value at the worst element: the output
     # rounding alone, part of every bf16 result's error
     half_ulp = 2.0 ** (np.floor(np.log2(max(abs(float(ref_o[at])), 1e-30))) - 8)
+    # the largest error beyond what storing the exact value as bf16 costs by
+    # itself: the kernel's own share
+    beyond = float(np.max(err - bf16_rounding(ref_o)))
     print(f"\nPARITY {what}: rows={rl.size} max_abs={err.max():.3e} mean_abs={err.mean():.3e} "
           f"lse_abs={le:.3e} oracle_s={oracle_s:.1f} |o| at worst={abs(float(ref_o[at])):.3f} "
-          f"(bf16 half-ulp {half_ulp:.2e})", flush=True)
+          f"(bf16 half-ulp {half_ulp:.2e}) beyond_output_rounding={beyond:.3e}", flush=True)
 
 
 def sample_rows(B, H, S, cp, n_per_head, seed, heads=None):
