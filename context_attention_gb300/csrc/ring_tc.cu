@@ -10,8 +10,9 @@
 // multiplied into V, and everything accumulates in fp32 across all steps.
 //
 // How (one GPU, GB300): a persistent kernel, one CTA per SM.  A work unit is
-// 256 query rows (two 128-row tiles) of one (batch, head, shard).  Warp
-// roles:
+// two 128-row query tiles of one (batch, shard): the same rows of two query
+// heads that share a KV head when the GQA group size is even, else two
+// consecutive row blocks of one head.  Warp roles:
 //   warps 0-3, 4-7   softmax warpgroups, one per query tile: each thread owns
 //                    one query row (one TMEM lane) -- it reads its S row from
 //                    TMEM, applies mask, shift and exp2, keeps the row sum in
@@ -103,9 +104,17 @@ constexpr int kMaxRanks = 8;               // segmented schedule
 
 struct TcParams {
   RingArgs a;
-  int qblocks;      // 256-row units per stored q shard
+  // A unit's two 128-row query tiles: the same rows of two query heads that
+  // share a KV head (hp = 1, when the GQA group size is even), else two
+  // consecutive row blocks of one head.  Paired heads see the same causal
+  // limits and the same K/V tiles, so neither tile runs key tiles that lie
+  // wholly past its diagonal; a 256-row unit's first tile runs one such
+  // tile per ring step.
+  int hp;
+  int unit_rows;    // query rows per unit and head: 128 (hp) or 256
+  int qblocks;      // units per stored q shard and head (slot)
   int64_t units;    // total work units
-  int64_t per_head; // units per (b, h)
+  int64_t per_head; // units per head slot: (b, h), or (b, head pair) when hp
   int nsteps;
   int nkt;          // key tiles per shard
   float scale_log2;
@@ -130,7 +139,7 @@ struct TcMaps {
 };
 
 struct Unit {
-  int64_t bh;
+  int64_t bh, bh1;  // b * Hq + head of query tile 0 and of query tile 1
   int b, h;
   int64_t bhk;
   int r_store, r_log;
@@ -143,20 +152,38 @@ struct Unit {
 // shard pair has a diagonal); non-causal units are all equal.
 __device__ __forceinline__ Unit unit_of(const TcParams& P, int64_t u) {
   Unit U;
-  U.bh = u / P.per_head;
+  const int64_t slot = u / P.per_head;  // (b, h) or (b, head pair)
   const int64_t rem = P.per_head - 1 - (u % P.per_head);
   if (P.a.causal && P.a.layout == kLayoutContiguous) {
     U.r_store = (int)(rem / P.qblocks);
-    U.qrow0 = (rem % P.qblocks) * kUnitRows;
+    U.qrow0 = (rem % P.qblocks) * P.unit_rows;
   } else {
     U.r_store = (int)(rem % P.a.q_shards);
-    U.qrow0 = (rem / P.a.q_shards) * kUnitRows;
+    U.qrow0 = (rem / P.a.q_shards) * P.unit_rows;
   }
-  U.b = (int)(U.bh / P.a.Hq);
-  U.h = (int)(U.bh % P.a.Hq);
+  if (P.hp) {
+    U.b = (int)(slot / (P.a.Hq / 2));
+    U.h = (int)(slot % (P.a.Hq / 2)) * 2;
+    U.bh = (int64_t)U.b * P.a.Hq + U.h;
+    U.bh1 = U.bh + 1;
+  } else {
+    U.bh = U.bh1 = slot;
+    U.b = (int)(slot / P.a.Hq);
+    U.h = (int)(slot % P.a.Hq);
+  }
   U.bhk = (int64_t)U.b * P.a.Hkv + U.h / (P.a.Hq / P.a.Hkv);
   U.r_log = P.a.q_rank_fixed >= 0 ? P.a.q_rank_fixed : U.r_store;
   return U;
+}
+
+// Head (b * Hq + h) and first local query row of query tile i of a unit.
+__device__ __forceinline__ int64_t tile_bh(const Unit& U, int i) { return i ? U.bh1 : U.bh; }
+__device__ __forceinline__ int64_t tile_row0(const TcParams& P, const Unit& U, int i) {
+  return U.qrow0 + (P.hp ? 0 : (int64_t)i * kBM);
+}
+// TMA row of query tile i's first row in the [B * Hq * Sq, D] view of q.
+__device__ __forceinline__ int tile_qrow(const TcParams& P, const Unit& U, int i) {
+  return (int)(tile_bh(U, i) * P.a.Sq + (int64_t)U.r_store * P.a.Ls + tile_row0(P, U, i));
 }
 
 // The k-th unit of this CTA: units are dealt to CTAs in a snake order
@@ -182,7 +209,7 @@ struct Step {
 
 __device__ __forceinline__ Step step_info(const TcParams& P, const Unit& U, int t) {
   Step st;
-  const int64_t a_max = min(U.qrow0 + kUnitRows - 1, P.a.Ls - 1);
+  const int64_t a_max = min(U.qrow0 + P.unit_rows - 1, P.a.Ls - 1);
   if (P.seg) {
     const int R = P.part_rank >= 0 ? P.part_rank : (t >> 1);
     st.rank = R;
@@ -748,18 +775,16 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         // Q tiles and K_0 on q_full
         mbar_arrive_expect_tx(bar(kBarQFull), 3 * kTileBytes);
         ++q_armed;
-        const int qrow = (int)(U.bh * P.a.Sq + (int64_t)U.r_store * P.a.Ls + U.qrow0);
         for (int i = 0; i < 2; ++i)
           for (int hx = 0; hx < 2; ++hx)
             tma_load_2d(sbase + kSmemQ + i * kTileBytes + hx * kBoxBytes, &maps.q, bar(kBarQFull),
-                        hx * 64, qrow + i * kBM);
+                        hx * 64, tile_qrow(P, U, i));
         load_kv(it.st, it.kt, 0, bar(kBarQFull));
         // the next unit's Q tiles come from HBM: start them towards L2 now
         if (unit_at(P, k + 1) < P.units) {
           const Unit N = unit_of(P, unit_at(P, k + 1));
-          const int nrow = (int)(N.bh * P.a.Sq + (int64_t)N.r_store * P.a.Ls + N.qrow0);
           for (int i = 0; i < 2; ++i)
-            for (int hx = 0; hx < 2; ++hx) tma_prefetch_2d(&maps.q, hx * 64, nrow + i * kBM);
+            for (int hx = 0; hx < 2; ++hx) tma_prefetch_2d(&maps.q, hx * 64, tile_qrow(P, N, i));
         }
         // V_j and K_(j+1) on the tile barrier of tile j.  The barrier's
         // previous phase (tile t - kNGroup) was waited for by the issuing
@@ -886,9 +911,9 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
     for (int64_t k = 0, u = unit_at(P, 0); u < P.units && ok; ++k, u = unit_at(P, k)) {
       const Unit U = unit_of(P, u);
       const int n = unit_tiles(P, U);
-      const int64_t a_row = U.qrow0 + (int64_t)i * kBM + tid;
+      const int64_t a_row = tile_row0(P, U, i) + tid;
       const bool valid = a_row < P.a.Ls;
-      const int64_t orow = U.bh * P.a.Sq + (int64_t)U.r_store * P.a.Ls + a_row;
+      const int64_t orow = tile_bh(U, i) * P.a.Sq + (int64_t)U.r_store * P.a.Ls + a_row;
       if (n == 0) {
         if (valid) {
           if (P.a.out_f32) {
@@ -1162,9 +1187,11 @@ static cudaError_t launch_tc(const TcMaps& maps, const TcParams& P, cudaStream_t
 
 static void init_common(TcParams& P, const RingArgs& a) {
   P.a = a;
-  P.qblocks = (int)((a.Ls + kUnitRows - 1) / kUnitRows);
+  P.hp = (a.Hq / a.Hkv) % 2 == 0;
+  P.unit_rows = P.hp ? kBM : kUnitRows;
+  P.qblocks = (int)((a.Ls + P.unit_rows - 1) / P.unit_rows);
   P.per_head = (int64_t)a.q_shards * P.qblocks;
-  P.units = (int64_t)a.B * a.Hq * P.per_head;
+  P.units = (int64_t)a.B * (P.hp ? a.Hq / 2 : a.Hq) * P.per_head;
   P.nkt = (int)((a.Ls + kBN - 1) / kBN);
   P.scale_log2 = a.scale * kLog2e;
   P.seg = 0;

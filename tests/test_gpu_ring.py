@@ -117,13 +117,17 @@ def test_bf16_small(ca, mode, causal, layout):
 
 @pytest.mark.parametrize("mode", ["online_max", "const_max"])
 @pytest.mark.parametrize("causal,layout", [(False, "contiguous"), (True, "contiguous"), (True, "striped")])
-def test_bf16_gqa_ragged(ca, mode, causal, layout):
-    """GQA 4:2 (kv head h//2), Ls = 300 (ragged: 3 key tiles, last one partial;
-    the second query tile of the last unit mostly empty), cp = 3, B = 2."""
-    q, k, v = gen(2, 4, 2, 900, 128, 4, torch.bfloat16)
+@pytest.mark.parametrize("G", [2, 3, 4])
+def test_bf16_gqa_ragged(ca, mode, causal, layout, G):
+    """GQA 2G:2 (kv head h//G), Ls = 300 (ragged: 3 key tiles, last one
+    partial), cp = 3, B = 2.  An even G pairs the same 128 rows of heads h
+    and h+1 in one unit (3 units per shard, the last mostly empty); G = 3
+    keeps two consecutive row blocks of one head (the second query tile of
+    the last unit mostly empty)."""
+    q, k, v = gen(2, 2 * G, 2, 900, 128, 4, torch.bfloat16)
     o, lse = ca.ring_attn_fwd(q, k, v, 3, mode=mode, causal=causal, layout=layout)
     ro, rl = oracle_ring(q, k, v, 3, mode, causal, layout)
-    assert_close(np32(o), ro, np32(lse), rl, what=f"bf16 gqa {mode} causal={causal} {layout}")
+    assert_close(np32(o), ro, np32(lse), rl, what=f"bf16 gqa G={G} {mode} causal={causal} {layout}")
 
 
 @pytest.mark.parametrize("S,cp", [(128, 1), (8, 8), (136, 8), (1, 1)])
@@ -224,6 +228,36 @@ def test_lse_merge_kernel(ca):
         o, lse = ca.lse_merge(torch.tensor(op, device="cuda"), torch.tensor(lp, device="cuda"), out_dtype=out_dtype)
         assert_close(np32(o), ro, np32(lse), rl, dtype=torch.float32 if out_dtype == torch.float32 else torch.bfloat16,
                      what=f"merge {out_dtype}")
+
+
+@pytest.mark.parametrize("n,R,D", [(3, 44000, 128), (2, 44000, 192)])
+def test_lse_merge_larger_than_l2(ca, n, R, D):
+    """Partials of more than 64 MB take the merge kernel that requests the
+    partial rows before the weights (the one HBM-bound callers get); it must
+    give the oracle's merge, online (with empty partials and an all-empty
+    row) and with a shared const-max bound: unnormalised sums o_i with
+    lse_i = c + ln l_i merge to what the oracle gives for the normalised
+    partials o_i / l_i."""
+    assert n * R * D * 4 > (64 << 20)
+    rng = np.random.default_rng(20 + D)
+    op = rng.standard_normal((n, R, D)).astype(np.float32)
+    lp = (rng.standard_normal((n, R)) * 3).astype(np.float32)
+    lp[0, ::5] = -np.inf
+    lp[:, 7] = -np.inf
+    ro, rl = oracle.lse_merge(op, lp)
+    for out_dtype in (torch.float32, torch.bfloat16):
+        o, lse = ca.lse_merge(torch.tensor(op, device="cuda"), torch.tensor(lp, device="cuda"), out_dtype=out_dtype)
+        assert_close(np32(o), ro, np32(lse), rl, dtype=torch.float32 if out_dtype == torch.float32 else torch.bfloat16,
+                     what=f"large merge {out_dtype}")
+    # const max: every row's bound c above its partials' lse, no empty rows
+    lc = (rng.standard_normal((n, R)) * 3).astype(np.float32)
+    c = (lc.max(axis=0) + 2.0).astype(np.float32)
+    l_i = np.exp(lc.astype(np.float64) - c.astype(np.float64))
+    unnorm = (op * l_i[:, :, None]).astype(np.float32)
+    ro, rl = oracle.lse_merge(unnorm.astype(np.float64) / l_i[:, :, None], lc)
+    o, lse = ca.lse_merge(torch.tensor(unnorm, device="cuda"), torch.tensor(lc, device="cuda"),
+                          c=torch.tensor(c, device="cuda"), out_dtype=torch.float32)
+    assert_close(np32(o), ro, np32(lse), rl, dtype=torch.float32, what="large const-max merge")
 
 
 def test_const_max_bound_kernel(ca):
