@@ -1011,7 +1011,14 @@ def run_ours(args):
     # failure there is reported in the line rather than losing the line
     if args.other_workloads or (world == 1 and not args.no_other_workloads):
         try:
-            out["other_workloads"] = bench_other_workloads(ca, torch, cpu_seconds=cpu_each)
+            ow = bench_other_workloads(ca, torch, cpu_seconds=cpu_each)
+            # each workload's rate against the same measured peaks as the headline
+            for w in ow.values():
+                if "tflops" in w:
+                    w["frac_of_burst_bf16"] = round(w["tflops"] / peaks["bf16_tflops"], 4)
+                if "gbs" in w:
+                    w["frac_of_copy_bw"] = round(w["gbs"] / peaks["hbm_gbs"], 4)
+            out["other_workloads"] = ow
         except Exception as e:  # noqa: BLE001 -- report, keep the headline
             out["other_workloads"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0 and not args.no_cpu_baseline:
