@@ -681,9 +681,10 @@ def causal_rank_imbalance(S, cp, layout):
 def bench_other_workloads(ca, torch, reps=5, cpu_seconds=None):
     """Device time of the other workloads (online max, sink keys, causal GQA
     in both layouts, the QKV prologue, DCP prefill, paged and Ring Pass-Q
-    decode) with the same CUDA-event method; each is reported with its
-    algorithmic rate (causal counts visible pairs).  With cpu_seconds, each
-    also gets the oracle timed on a sample of about that many seconds."""
+    decode, DCP decode of one and two sequences) with the same CUDA-event
+    method; each is reported with its algorithmic rate (causal counts
+    visible pairs).  With cpu_seconds, each also gets the oracle timed on a
+    sample of about that many seconds."""
     from context_attention_gb300 import synth
 
     res = {}
@@ -840,6 +841,31 @@ def bench_other_workloads(ca, torch, reps=5, cpu_seconds=None):
             q, kr, vr, 8, "striped", cpu_seconds)
     del q, kr, vr
     torch.cuda.empty_cache()
+    # small-batch DCP decode: one and two of the decode workload's sequences
+    # (537 MB and 1.07 GB of K/V, more than L2; launches back to back)
+    for nseq in (1, 2):
+        q, kd, vd = synth.decode_inputs(nseq, d["Hq"], d["Hkv"], d["D"], d["W"], d["Lloc"], 8 + nseq,
+                                        device="cuda")
+        out = torch.empty_like(q)
+        lse = torch.empty(nseq, d["Hq"], device="cuda", dtype=torch.float32)
+        ws = torch.empty(ca.dcp_decode_workspace_size(nseq, d["Hq"], d["Hkv"], d["Lloc"], d["D"], d["W"], d["I"]),
+                         dtype=torch.uint8, device="cuda")
+        for _ in range(3):
+            ca.dcp_decode(q, kd, vd, d["I"], out=out, lse=lse, workspace=ws)
+        n_launch = 20 * reps
+        a.record(stream)
+        for _ in range(n_launch):
+            ca.dcp_decode(q, kd, vd, d["I"], out=out, lse=lse, workspace=ws)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / n_launch
+        nbytes = 2.0 * d["W"] * nseq * d["Hkv"] * d["Lloc"] * d["D"] * 2
+        name = f"dcp_decode {nseq}seq L131072 dcp4"
+        res[name] = {"ms": round(ms, 4), "gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
+        if cpu_seconds:
+            res[name]["cpu_baseline"] = oracle_dcp_decode_baseline(q, kd, vd, d["I"], cpu_seconds)
+        del q, kd, vd
+        torch.cuda.empty_cache()
     return res
 
 
@@ -885,24 +911,27 @@ def run_profile_case(args):
         for _ in range(args.warmup + 1):
             ca.lse_merge(o_parts, lse_parts, out_dtype=torch.bfloat16)
     elif args.profile == "paged":
-        # paged decode with 4 sequences in 16-slot blocks under a random block
-        # table: K+V 2.1 GB (> L2), one launch ~0.3 ms
+        # paged decode with 8 sequences (256 shard x sequence x KV-head pairs,
+        # dealt in splits as the 64-sequence workload is) in 16-slot blocks
+        # under a random block table: K+V 4.3 GB (> L2), one launch ~0.6 ms
         d = DECODE
-        q, kd, vd = synth.decode_inputs(4, d["Hq"], d["Hkv"], d["D"], d["W"], d["Lloc"], d["seed"], device="cuda")
+        ns = 8
+        q, kd, vd = synth.decode_inputs(ns, d["Hq"], d["Hkv"], d["D"], d["W"], d["Lloc"], d["seed"], device="cuda")
         bs, mb = 16, d["Lloc"] // 16
         g = torch.Generator(device="cuda")
         g.manual_seed(7)
-        perm = torch.stack([torch.randperm(4 * mb, generator=g, device="cuda") for _ in range(d["W"])])
-        kc = torch.empty(d["W"], 4 * mb, d["Hkv"], bs, d["D"], device="cuda", dtype=torch.bfloat16)
+        perm = torch.stack([torch.randperm(ns * mb, generator=g, device="cuda") for _ in range(d["W"])])
+        kc = torch.empty(d["W"], ns * mb, d["Hkv"], bs, d["D"], device="cuda", dtype=torch.bfloat16)
         vc = torch.empty_like(kc)
         for src, dst in ((kd, kc), (vd, vc)):
-            blocks = src.view(d["W"], 4, d["Hkv"], mb, bs, d["D"]).permute(0, 1, 3, 2, 4, 5).reshape(
-                d["W"], 4 * mb, d["Hkv"], bs, d["D"])
+            blocks = src.view(d["W"], ns, d["Hkv"], mb, bs, d["D"]).permute(0, 1, 3, 2, 4, 5).reshape(
+                d["W"], ns * mb, d["Hkv"], bs, d["D"])
             for r in range(d["W"]):
                 dst[r].index_copy_(0, perm[r], blocks[r])
-        bt = perm.view(d["W"], 4, mb).to(torch.int32).contiguous()
-        del kd, vd
-        sl = torch.full((4,), d["W"] * d["Lloc"], dtype=torch.int32, device="cuda")
+        bt = perm.view(d["W"], ns, mb).to(torch.int32).contiguous()
+        del kd, vd, blocks
+        torch.cuda.empty_cache()
+        sl = torch.full((ns,), d["W"] * d["Lloc"], dtype=torch.int32, device="cuda")
         for _ in range(args.warmup + 1):
             ca.dcp_decode_paged(q, kc, vc, bt, d["I"], sl)
     elif args.profile == "ring_decode":
@@ -918,9 +947,12 @@ def run_profile_case(args):
         for _ in range(args.warmup + 1):
             ca.ring_decode(q, kr, vr, 8, layout="striped")
     else:
-        # decode recipe with 4 sequences: K+V 2.1 GB (> L2), one launch ~0.3 ms
+        # decode recipe with 8 sequences (256 pairs, dealt in splits as the
+        # 64-sequence workload is): K+V 4.3 GB (> L2), one launch ~0.6 ms;
+        # decode_small: one sequence (contiguous ranges), 537 MB, ~90 us
         d = DECODE
-        q, kd, vd = synth.decode_inputs(4, d["Hq"], d["Hkv"], d["D"], d["W"], d["Lloc"], d["seed"], device="cuda")
+        ns = 1 if args.profile == "decode_small" else 8
+        q, kd, vd = synth.decode_inputs(ns, d["Hq"], d["Hkv"], d["D"], d["W"], d["Lloc"], d["seed"], device="cuda")
         for _ in range(args.warmup + 1):
             ca.dcp_decode(q, kd, vd, d["I"])
     torch.cuda.synchronize()
@@ -1089,7 +1121,8 @@ def main():
                     help="oracle seconds of the headline workload's CPU baseline")
     ap.add_argument("--cpu-seconds-each", type=float, default=3.0,
                     help="oracle seconds of each other workload's CPU baseline (decode and other_workloads)")
-    ap.add_argument("--profile", choices=["ring", "decode", "prologue", "key_pass", "merge", "paged", "ring_decode"],
+    ap.add_argument("--profile", choices=["ring", "decode", "decode_small", "prologue", "key_pass", "merge", "paged",
+                                          "ring_decode"],
                     default=None,
                     help="run one small launch of one kernel (for ncu captures) and exit")
     args = ap.parse_args()

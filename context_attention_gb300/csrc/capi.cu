@@ -390,10 +390,8 @@ size_t ca_dcp_decode_workspace_size(int N, int Hq, int Hkv, int64_t Lloc, int D,
                                     int interleave) {
   (void)interleave;
   if (N <= 0 || Hq <= 0 || Hkv <= 0 || Lloc <= 0 || D <= 0 || dcp <= 0) return 0;
-  int64_t chunk;
-  int splits;
-  dcp_decode_split(Lloc, &chunk, &splits);
-  const size_t parts = (size_t)dcp * splits;
+  const DecodeGeometry g = dcp_decode_geometry((int64_t)dcp * N * Hkv, Lloc, kDecodeMaxCtas);
+  const size_t parts = (size_t)dcp * g.slots;
   return align256(sizeof(float) * parts * N * Hq * D) + align256(sizeof(float) * parts * N * Hq);
 }
 
@@ -416,7 +414,6 @@ static DecodeArgs decode_args(const void* q, const void* k, const void* v, int N
   a.Lloc = Lloc;
   a.seq_lens = seq_lens;
   a.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
-  dcp_decode_split(Lloc, &a.chunk, &a.splits);
   a.paged = 0;
   a.block_tables = nullptr;
   a.nblk = a.max_blocks = 0;
@@ -429,7 +426,16 @@ static ca_status decode_run(DecodeArgs& a, void* workspace, void* o, float* lse,
   if (st != CA_OK) return st;
   unsigned* err = device_error_word();
   if (!err) return CA_ERR_CUDA;
-  const size_t parts = (size_t)a.W * a.splits;
+  const int sms = device_sm_count();
+  if (sms <= 0) return CA_ERR_CUDA;
+  const DecodeGeometry g = dcp_decode_geometry((int64_t)a.W * a.N * a.Hkv, a.Lloc,
+                                               sms < kDecodeMaxCtas ? sms : kDecodeMaxCtas);
+  a.stages = g.stages;
+  a.ctas = g.ctas;
+  a.slots = g.slots;
+  a.dealt = g.dealt;
+  a.split_stages = g.split_stages;
+  const size_t parts = (size_t)a.W * a.slots;
   a.o_parts = static_cast<float*>(workspace);
   a.lse_parts = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                          align256(sizeof(float) * parts * a.N * a.Hq * a.D));
@@ -457,10 +463,9 @@ ca_status ca_dcp_decode(const void* q, const void* k_shards, const void* v_shard
 
 size_t ca_ring_decode_workspace_size(int B, int Hq, int Hkv, int64_t S, int D, int cp_size) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || cp_size <= 0 || S % cp_size != 0) return 0;
-  int64_t chunk;
-  int splits;
-  dcp_decode_split(S / cp_size, &chunk, &splits);
-  const size_t parts = (size_t)cp_size * splits;
+  const DecodeGeometry g =
+      dcp_decode_geometry((int64_t)cp_size * B * Hkv, S / cp_size, kDecodeMaxCtas);
+  const size_t parts = (size_t)cp_size * g.slots;
   return align256(sizeof(float) * parts * B * Hq * D) + align256(sizeof(float) * parts * B * Hq);
 }
 

@@ -10,10 +10,23 @@
 // of them is visible to the decoded token (its own K/V sits on its owner).
 //
 // One GPU holds all shards (dcp ranks, or the cp shards of the ring layout,
-// whose valid slots and rows differ only in item_of).  A work item is (shard
-// r, sequence n, KV head, split of the shard's valid slots).  The scan is HBM
-// bound: a TMA producer warp streams 128-token stages (K and V, 64 KB) through
-// a 3-stage ring; four consumer warps each take 32 tokens of a stage.  The G
+// whose valid slots and rows differ only in pair_of and seg_tokens).  The
+// work is the 128-token stages of every (shard r, sequence n, KV head) pair,
+// cut into segments, each one CTA's share of one pair (SegWalk):
+//  - with many pairs, each pair's stages form splits of 32 stages (4096
+//    tokens) dealt to the CTAs round robin, so the CTAs stream neighbouring
+//    parts of the cache at any moment (at 64 sequences, contiguous ranges
+//    over the whole cache measured 1-2 % slower);
+//  - with few pairs (a handful of sequences), the stages, pair after pair,
+//    are cut into one contiguous range per CTA, the ranges differing by at
+//    most one stage.  Dealt splits left 104 of 152 CTAs a second 4096-token
+//    split at one sequence, where a CTA streams at most ~60 GB/s: the
+//    ranges took two sequences from 172.7 to 160.4 us and one from 92.8 to
+//    88.7 us.
+// Each segment yields one partial per query head, in its pair's slot.  The
+// scan is HBM bound: a TMA producer warp streams 128-token stages (K and V,
+// 64 KB, each one box holding both 64-column halves of its rows) through a
+// 3-stage ring; four consumer warps each take 32 tokens of a stage.  The G
 // query heads that share a KV head are the N side of warp-level bf16 MMAs
 // (m16n8k16, fp32 accumulate): S^T = K Q^T per 16 tokens, then O^T += V^T P^T,
 // with P moved from the accumulator layout to the operand layout by
@@ -23,7 +36,7 @@
 // as computed (for the log-sum-exp) and of p rounded to bf16 as the PV MMA
 // consumes it (O is divided by this one, so the weights in O and in its
 // normaliser are the same and o is a convex combination of V rows).  At the
-// end of an item the four warps' partial states are LSE-merged in shared
+// end of a segment the four warps' partial states are LSE-merged in shared
 // memory and one partial (o, lse) per query head is written.
 #include <atomic>
 #include <cuda.h>
@@ -64,7 +77,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 struct DecParams {
   DecodeArgs a;
   int G;
-  int64_t items;
+  int64_t units;  // pairs * stages
   float scale_log2;
 };
 
@@ -92,32 +105,90 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-struct Item {
-  int r, n, hkv, split;
-  int64_t t0, ntok;  // first valid local slot of the item, number of tokens
-  int64_t row0;      // first row of the item in the [W*N*Hkv*Lloc, D] view
+// One CTA's share of one pair: stages [s0, s1) of pair p, i.e. the pair's
+// local slots [t0, t0 + ntok) that hold tokens (none when the segment lies
+// past the shard's valid length).
+struct Seg {
+  int r, n, hkv;
+  int64_t t0, ntok;  // first local slot, number of valid tokens
+  int64_t row0;      // first row in the [W*N*Hkv*Lloc, D] view (contiguous caches)
+  int slot;          // partial slot of the segment within its pair
+  bool last;         // the segment ends the pair (its CTA writes the unused slots)
 };
 
-__device__ __forceinline__ Item item_of(const DecParams& P, int64_t it) {
+// CTA c deals with units [c * U / C, (c + 1) * U / C); unit x is on CTA
+// ((x + 1) * C - 1) / U, the last c whose range starts at or before x.
+__device__ __forceinline__ int64_t range_begin(int64_t U, int C, int64_t c) { return c * U / C; }
+__device__ __forceinline__ int64_t cta_of_unit(int64_t U, int C, int64_t x) {
+  return ((x + 1) * C - 1) / U;
+}
+
+// The pair's valid local slots and first cache row of its slot t0.
+__device__ __forceinline__ void pair_of(const DecParams& P, int64_t pair, Seg& S, int64_t* valid) {
   const DecodeArgs& a = P.a;
-  Item I;
-  I.split = (int)(it % a.splits);
-  int64_t rest = it / a.splits;
-  I.hkv = (int)(rest % a.Hkv);
-  rest /= a.Hkv;
-  I.n = (int)(rest % a.N);
-  I.r = (int)(rest / a.N);
-  const int64_t seq = a.seq_lens ? (int64_t)a.seq_lens[I.n] : (int64_t)a.W * a.Lloc;
-  int64_t valid = a.ring_layout < 0 ? dcp_local_filled(seq, a.W, a.I, a.I, I.r)
-                                    : ring_shard_filled(seq, a.W, a.Lloc, a.ring_layout, I.r);
-  if (valid > a.Lloc) valid = a.Lloc;
-  I.t0 = (int64_t)I.split * a.chunk;
-  I.ntok = valid - I.t0;
-  if (I.ntok > a.chunk) I.ntok = a.chunk;
-  if (I.ntok < 0) I.ntok = 0;
-  I.row0 = a.ring_layout < 0 ? (((int64_t)I.r * a.N + I.n) * a.Hkv + I.hkv) * a.Lloc + I.t0
-                              : (((int64_t)I.n * a.Hkv + I.hkv) * a.W + I.r) * a.Lloc + I.t0;
-  return I;
+  S.hkv = (int)(pair % a.Hkv);
+  const int64_t rest = pair / a.Hkv;
+  S.n = (int)(rest % a.N);
+  S.r = (int)(rest / a.N);
+  const int64_t seq = a.seq_lens ? (int64_t)a.seq_lens[S.n] : (int64_t)a.W * a.Lloc;
+  int64_t v = a.ring_layout < 0 ? dcp_local_filled(seq, a.W, a.I, a.I, S.r)
+                                : ring_shard_filled(seq, a.W, a.Lloc, a.ring_layout, S.r);
+  *valid = v > a.Lloc ? a.Lloc : v;
+}
+
+// Segment stages [s0, s1) of the pair: tokens [s0 * 128, min(s1 * 128, valid)).
+__device__ __forceinline__ void seg_tokens(const DecParams& P, int64_t s0, int64_t s1, int64_t valid,
+                                           Seg& S) {
+  const DecodeArgs& a = P.a;
+  S.t0 = s0 * kTok;
+  const int64_t t1 = s1 * kTok < valid ? s1 * kTok : valid;
+  S.ntok = t1 > S.t0 ? t1 - S.t0 : 0;
+  S.row0 = a.ring_layout < 0 ? (((int64_t)S.r * a.N + S.n) * a.Hkv + S.hkv) * a.Lloc + S.t0
+                              : (((int64_t)S.n * a.Hkv + S.hkv) * a.W + S.r) * a.Lloc + S.t0;
+}
+
+// Walks one CTA's segments in order; the producer and the consumers each
+// run one and see the same sequence.
+struct SegWalk {
+  int64_t u, u_end;
+};
+__device__ __forceinline__ SegWalk seg_walk(const DecParams& P) {
+  const DecodeArgs& a = P.a;
+  SegWalk w;
+  if (a.dealt) {
+    w.u = blockIdx.x;
+    w.u_end = P.units;
+  } else {
+    w.u = range_begin(P.units, a.ctas, blockIdx.x);
+    w.u_end = range_begin(P.units, a.ctas, blockIdx.x + 1);
+  }
+  return w;
+}
+__device__ __forceinline__ bool seg_next(const DecParams& P, SegWalk& w, Seg& S) {
+  if (w.u >= w.u_end) return false;
+  const DecodeArgs& a = P.a;
+  int64_t valid;
+  if (a.dealt) {
+    // unit = (pair, split): a split of split_stages stages, its own slot
+    const int64_t pair = w.u / a.slots, split = w.u % a.slots;
+    pair_of(P, pair, S, &valid);
+    const int64_t s0 = split * a.split_stages;
+    const int64_t s1 = s0 + a.split_stages < a.stages ? s0 + a.split_stages : a.stages;
+    seg_tokens(P, s0, s1, valid, S);
+    S.slot = (int)split;
+    S.last = false;
+    w.u += a.ctas;
+    return true;
+  }
+  const int64_t SP = a.stages;
+  const int64_t pair = w.u / SP, pu0 = pair * SP;
+  const int64_t s1u = w.u_end < pu0 + SP ? w.u_end : pu0 + SP;
+  pair_of(P, pair, S, &valid);
+  seg_tokens(P, w.u - pu0, s1u - pu0, valid, S);
+  S.slot = (int)(blockIdx.x - cta_of_unit(P.units, a.ctas, pu0));
+  S.last = s1u == pu0 + SP;
+  w.u = s1u;
+  return true;
 }
 
 template <bool kPaged>
@@ -165,8 +236,9 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
     const uint32_t box_bytes = (uint32_t)a.bs * 128;
     uint64_t pos = 0;
     bool ok = true;
-    for (int64_t it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
-      const Item I = item_of(P, it);
+    SegWalk walk = seg_walk(P);
+    Seg I;
+    while (ok && seg_next(P, walk, I)) {
       const int nst = (int)((I.ntok + kTok - 1) / kTok);
       const int32_t* bt = a.block_tables + ((int64_t)I.r * a.N + I.n) * a.max_blocks;
       for (int st = 0; st < nst; ++st) {
@@ -206,8 +278,9 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
       const uint64_t policy = l2_policy_evict_first();
       uint64_t pos = 0;
       bool ok = true;
-      for (int64_t it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
-        const Item I = item_of(P, it);
+      SegWalk walk = seg_walk(P);
+      Seg I;
+      while (ok && seg_next(P, walk, I)) {
         const int nst = (int)((I.ntok + kTok - 1) / kTok);
         for (int st = 0; st < nst; ++st) {
           const int slot = (int)(pos % kStages);
@@ -216,10 +289,8 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
           mbar_arrive_expect_tx(full(slot), kStageBytes);
           const int row = (int)(I.row0 + (int64_t)st * kTok);
           const uint32_t dst = sbase + kSmemStages + slot * kStageBytes;
-          tma_load_2d_hint(dst + 0 * kBox, &tk, full(slot), 0, row, policy);
-          tma_load_2d_hint(dst + 1 * kBox, &tk, full(slot), 64, row, policy);
-          tma_load_2d_hint(dst + 2 * kBox, &tv, full(slot), 0, row, policy);
-          tma_load_2d_hint(dst + 3 * kBox, &tv, full(slot), 64, row, policy);
+          tma_load_3d_hint(dst, &tk, full(slot), 0, row, 0, policy);
+          tma_load_3d_hint(dst + 2 * kBox, &tv, full(slot), 0, row, 0, policy);
           ++pos;
         }
       }
@@ -236,10 +307,11 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
     const int G = P.G;
     // Where token tok's 64-column half h sits in a stage's K (or V) region:
     // (tok + (tok & bmask)) * 128 + h * hstride, each 128-byte row swizzled
-    // (16-byte chunk c stored at c ^ (tok & 7)).  Contiguous caches load one
-    // box per half of the whole stage: bmask 0, hstride = kBox.  Paged caches
-    // load one box per block holding both halves of its bs rows, [half][row]:
-    // bmask = ~(bs - 1), hstride = bs * 128.
+    // (16-byte chunk c stored at c ^ (tok & 7)).  Both kinds of cache load
+    // boxes holding both 64-column halves of their rows, [half][row]:
+    // contiguous caches one box for the stage's 128 rows (bmask 0, hstride =
+    // kBox), paged caches one per block of bs rows (bmask = ~(bs - 1),
+    // hstride = bs * 128).
     const int bmask = kPaged ? ~(a.bs - 1) : 0;
     const uint32_t hstride = kPaged ? (uint32_t)a.bs * 128 : kBox;
     auto half_row = [&](int tok, int h) {
@@ -248,17 +320,34 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
     uint64_t pos = 0;
     uint32_t merges = 0;  // phases completed on merge_bar
     bool ok = true;
-    for (int64_t it = blockIdx.x; it < P.items && ok; it += gridDim.x) {
-      const Item I = item_of(P, it);
-      const int pidx = I.r * a.splits + I.split;
+    SegWalk walk = seg_walk(P);
+    Seg I;
+    while (ok && seg_next(P, walk, I)) {
       const int64_t R = (int64_t)a.N * a.Hq;
       const int64_t orow0 = (int64_t)I.n * a.Hq + (int64_t)I.hkv * G;  // first q head row
-      if (I.ntok == 0) {
-        for (int idx = threadIdx.x; idx < G * kD; idx += kConsumerWarps * 32) {
-          const int h = idx / kD, d = idx % kD;
-          a.o_parts[((int64_t)pidx * R + orow0 + h) * kD + d] = 0.f;
-          if (d == 0) a.lse_parts[(int64_t)pidx * R + orow0 + h] = -INFINITY;
+      if (I.slot < 0 || I.slot >= a.slots) {
+        // a slot outside the pair's bound (the host sized it otherwise):
+        // reported, nothing written
+        if (threadIdx.x == 0) {
+          *abort_flag = 1;
+          atomicOr(err, kErrBadLaunch);
         }
+        ok = false;
+        break;
+      }
+      const int pidx = I.r * a.slots + I.slot;
+      // the pair's slots that no segment reaches carry no weight
+      if (I.last) {
+        for (int idx = threadIdx.x; idx < (a.slots - 1 - I.slot) * G; idx += kConsumerWarps * 32) {
+          const int sl = I.slot + 1 + idx / G, h = idx % G;
+          a.lse_parts[((int64_t)I.r * a.slots + sl) * R + orow0 + h] = -INFINITY;
+        }
+      }
+      if (I.ntok == 0) {
+        // no valid token in the segment: a partial of no weight (the merge
+        // does not read the o row of a partial whose lse is -inf)
+        for (int h = threadIdx.x; h < G; h += kConsumerWarps * 32)
+          a.lse_parts[(int64_t)pidx * R + orow0 + h] = -INFINITY;
         continue;
       }
       // Q^T operand fragments (B of S^T = K Q^T): head g, d = 16kk + 2t (+8)
@@ -426,7 +515,7 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
         a.o_parts[prow * kD + d] = L > 0.f ? O / Lr : 0.f;
         if (d == 0) a.lse_parts[prow] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
       }
-      // every warp has read the shared partials before the next item rewrites them
+      // every warp has read the shared partials before the next segment rewrites them
       __syncwarp();
       if (lane == 0) mbar_arrive(merge_bar);
       ok = __all_sync(0xffffffffu, mbar_wait(merge_bar, merges & 1, abort_flag, err));
@@ -438,13 +527,30 @@ dcp_decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant_
 
 }  // namespace
 
-void dcp_decode_split(int64_t Lloc, int64_t* chunk, int* splits) {
-  int64_t c = 4096;
-  const int64_t lr = (Lloc + kTok - 1) / kTok * kTok;
-  if (lr < c) c = lr < kTok ? kTok : lr;
-  *chunk = c;
-  *splits = (int)((Lloc + c - 1) / c);
-  if (*splits < 1) *splits = 1;
+DecodeGeometry dcp_decode_geometry(int64_t pairs, int64_t Lloc, int max_ctas) {
+  DecodeGeometry g;
+  g.stages = (Lloc + kTok - 1) / kTok;
+  g.dealt = pairs >= kDecodeDealPairs;
+  g.split_stages = 32;  // 4096 tokens
+  if (g.dealt) {
+    g.slots = (int)((g.stages + g.split_stages - 1) / g.split_stages);
+    g.units = pairs * g.slots;
+  } else {
+    g.units = pairs * g.stages;
+  }
+  const int64_t c = g.units < max_ctas ? g.units : max_ctas;
+  g.ctas = (int)(c > 0 ? c : 0);
+  if (g.dealt) return g;
+  if (g.ctas == 0) {
+    g.slots = 1;
+    return g;
+  }
+  // every range holds at least U / C units, so a pair of SP units meets at
+  // most (SP - 2) / (U / C) + 2 ranges: one at each end, the rest inside it
+  const int64_t minlen = g.units / g.ctas;
+  g.slots = (int)((g.stages - 1) / minlen + 2);
+  if (g.slots > g.stages) g.slots = (int)g.stages;
+  return g;
 }
 
 template <bool kPaged>
@@ -459,9 +565,7 @@ static cudaError_t launch_decode(const DecParams& P, const CUtensorMap& tk, cons
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
-  const int sms = device_sm_count();
-  const int64_t grid = P.items < sms ? P.items : sms;
-  dcp_decode_kernel<kPaged><<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(tk, tv, P);
+  dcp_decode_kernel<kPaged><<<(unsigned)P.a.ctas, kThreads, kSmemAlloc, stream>>>(tk, tv, P);
   return cudaGetLastError();
 }
 
@@ -469,9 +573,9 @@ cudaError_t launch_dcp_decode_partials(const DecodeArgs& a, cudaStream_t stream)
   DecParams P;
   P.a = a;
   P.G = a.Hq / a.Hkv;
-  P.items = (int64_t)a.W * a.N * a.Hkv * a.splits;
+  P.units = (int64_t)a.W * a.N * a.Hkv * (a.dealt ? a.slots : a.stages);
   P.scale_log2 = a.scale * kLog2e;
-  if (P.items == 0) return cudaSuccess;
+  if (P.units == 0 || a.ctas <= 0) return cudaSuccess;
   CUtensorMap tk, tv;
   if (a.paged) {
     const uint64_t rows = (uint64_t)a.W * a.nblk * a.Hkv * a.bs;
@@ -482,8 +586,8 @@ cudaError_t launch_dcp_decode_partials(const DecodeArgs& a, cudaStream_t stream)
     return launch_decode<true>(P, tk, tv, stream);
   }
   const uint64_t rows = (uint64_t)a.W * a.N * a.Hkv * a.Lloc;
-  if (!encode_bf16_2d_sw128(&tk, a.k, rows, kD, kTok, 64) ||
-      !encode_bf16_2d_sw128(&tv, a.v, rows, kD, kTok, 64))
+  if (!encode_bf16_halves_sw128(&tk, a.k, rows, (uint32_t)kTok) ||
+      !encode_bf16_halves_sw128(&tv, a.v, rows, (uint32_t)kTok))
     return cudaErrorInvalidValue;
   return launch_decode<false>(P, tk, tv, stream);
 }

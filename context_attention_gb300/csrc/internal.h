@@ -81,10 +81,13 @@ struct DecodeArgs {
   int64_t Lloc;
   const int32_t* seq_lens;  // [N] or null
   float scale;
-  int splits;             // partials per shard
-  int64_t chunk;          // tokens per split (multiple of 128)
-  float* o_parts;         // [W*splits, N*Hq, D]
-  float* lse_parts;       // [W*splits, N*Hq]
+  int64_t stages;         // 128-token stages per (shard, sequence, KV head) pair
+  int ctas;               // CTAs of the partial kernel
+  int slots;              // partial slots per pair: W * slots partials per query row
+  int dealt;              // 1: pairs' splits dealt round robin; 0: contiguous ranges
+  int64_t split_stages;   // stages per split when dealt
+  float* o_parts;         // [W*slots, N*Hq, D]
+  float* lse_parts;       // [W*slots, N*Hq]
   unsigned* err;
   // paged cache (k, v are [W, nblk, Hkv, bs, D]; Lloc = max_blocks * bs)
   int paged;
@@ -96,8 +99,29 @@ struct DecodeArgs {
   int ring_layout = -1;
 };
 cudaError_t launch_dcp_decode_partials(const DecodeArgs& a, cudaStream_t stream);
-// Decode split geometry shared by the workspace query and the launch.
-void dcp_decode_split(int64_t Lloc, int64_t* chunk, int* splits);
+// Decode work geometry shared by the workspace query and the launch.  With
+// many (shard, sequence, KV head) pairs (kDecodeDealPairs or more) each
+// pair's 128-token stages form splits of up to 32 stages that are dealt to
+// the CTAs round robin, one partial per split: the CTAs then stream
+// neighbouring parts of the cache at any moment.  With fewer pairs the
+// stages, pair after pair, are cut into `ctas` contiguous ranges whose
+// lengths differ by at most one stage; a CTA writes one partial for each
+// pair its range meets, into the pair's slot numbered by its CTA index minus
+// that of the pair's first CTA, and `slots` bounds how many ranges one pair
+// can meet.  The workspace query takes max_ctas = kDecodeMaxCtas, an upper
+// bound of every launch's count, so it never sizes for fewer slots than a
+// launch uses.
+constexpr int kDecodeMaxCtas = 256;
+constexpr int64_t kDecodeDealPairs = 256;
+struct DecodeGeometry {
+  int64_t stages;        // stages per pair
+  int64_t units;         // pairs * stages (contiguous) or pairs * splits (dealt)
+  int ctas;
+  int slots;
+  int dealt;
+  int64_t split_stages;  // dealt: stages per split
+};
+DecodeGeometry dcp_decode_geometry(int64_t pairs, int64_t Lloc, int max_ctas);
 
 cudaError_t launch_paged_kv_write(const void* k_new, const void* v_new, const int64_t* slots,
                                   void* k_cache, void* v_cache, int T, int Hkv, int D, int W,

@@ -181,6 +181,9 @@ ca_status ca_attn_partial_step(const void *q_shard, const void *k_shard,
  *             sums of ca_attn_partial_step; acc_l_i = exp(lse_i - c),
  *             o = sum_i o_i / max(sum_i acc_l_i, 1e-37), lse = c + ln sum_i
  *             acc_l_i (pure addition).
+ * A partial of zero weight (lse_i = -inf in either mode, or, with c ==
+ * NULL, a weight that underflows to 0) adds nothing: its o row is not used
+ * and may hold any bits, NaN included.
  * o           device [R, D] of out_dtype; lse device [R] fp32 or NULL.
  * ---------------------------------------------------------------------- */
 ca_status ca_lse_merge(const float *o_parts, const float *lse_parts, int n,
@@ -297,8 +300,9 @@ ca_status ca_dcp_decode(const void *q, const void *k_shards,
  * after cudaDeviceReset are unsupported); make that first call before any
  * stream capture.  All calls on a device share the one scratch array, so
  * calls whose kernels overlap on the GPU race on it and must be serialised
- * by the caller.  Nothing in it needs to start at zero: every partial the
- * merge reads is written by the same call. */
+ * by the caller.  Nothing in it needs to start at zero: the same call writes
+ * the log-sum-exp of every partial slot, and the o row of every slot that
+ * holds tokens (the merge does not use the others). */
 ca_status ca_dcp_decode_noalloc(const void *q, const void *k_shards,
                                 const void *v_shards, ca_dtype dtype, int N,
                                 int Hq, int Hkv, int64_t Lloc, int D, int dcp,

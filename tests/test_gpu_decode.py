@@ -66,6 +66,51 @@ def test_decode_multi_split_and_garbage_tail(ca):
     assert_close(np32(o), ro, np32(lse), rl, what="decode nan tail")
 
 
+@pytest.mark.parametrize("N", [7, 8])
+def test_decode_contiguous_ranges_and_dealt_splits(ca, N):
+    """224 (shard, sequence, KV head) pairs are cut into one contiguous range
+    of stages per CTA, 256 are dealt as 4096-token splits: both must give the
+    oracle's decode, with lengths that leave shards empty, end mid-stage and
+    fill the cache, and NaN in every slot past a shard's valid count."""
+    from context_attention_gb300 import synth
+
+    Hq, Hkv, W, I, Lloc = 16, 8, 4, 16, 2560 + 1280
+    q, k, v = synth.decode_inputs(N, Hq, Hkv, 128, W, Lloc, 60 + N, device="cuda")
+    lens = [0, 1, 129, 5000, W * Lloc, 12345, 7, 9999][:N]
+    for r in range(W):
+        for n in range(N):
+            lf = ca.dcp_local_filled(lens[n], W, I, I, r)
+            k[r, n, :, lf:] = float("nan")
+            v[r, n, :, lf:] = float("nan")
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    o, lse = ca.dcp_decode(q, k, v, I, seq_lens=sl)
+    ro, rl = oracle.dcp_decode(np32(q), np32(torch.nan_to_num(k)), np32(torch.nan_to_num(v)), I, seq_lens=lens)
+    assert_close(np32(o), ro, np32(lse), rl, what=f"decode, {W * N * Hkv} pairs")
+
+
+def test_decode_one_sequence_131k(ca):
+    """One sequence over four 32768-slot shards (the small-batch decode): the
+    32 pairs' 1024 stages split into one range per CTA, so a pair's stages
+    meet several CTAs and its partial slots fill from several of them; a
+    second length ends mid-stage with NaN past it."""
+    from context_attention_gb300 import synth
+
+    N, Hq, Hkv, W, I, Lloc = 1, 32, 8, 4, 16, 32768
+    q, k, v = synth.decode_inputs(N, Hq, Hkv, 128, W, Lloc, 70, device="cuda")
+    o, lse = ca.dcp_decode(q, k, v, I)
+    ro, rl = oracle.dcp_decode(np32(q), np32(k), np32(v), I)
+    assert_close(np32(o), ro, np32(lse), rl, what="decode, one sequence of 131072 tokens")
+    L = 100001
+    for r in range(W):
+        lf = ca.dcp_local_filled(L, W, I, I, r)
+        k[r, 0, :, lf:] = float("nan")
+        v[r, 0, :, lf:] = float("nan")
+    sl = torch.tensor([L], dtype=torch.int32, device="cuda")
+    o, lse = ca.dcp_decode(q, k, v, I, seq_lens=sl)
+    ro, rl = oracle.dcp_decode(np32(q), np32(torch.nan_to_num(k)), np32(torch.nan_to_num(v)), I, seq_lens=[L])
+    assert_close(np32(o), ro, np32(lse), rl, what="decode, one sequence of 100001 tokens")
+
+
 def test_decode_zero_length_sequence(ca):
     """seq_len = 0: every partial is empty: o = 0, lse = -inf."""
     from context_attention_gb300 import synth

@@ -260,6 +260,42 @@ def test_lse_merge_larger_than_l2(ca, n, R, D):
     assert_close(np32(o), ro, np32(lse), rl, dtype=torch.float32, what="large const-max merge")
 
 
+@pytest.mark.parametrize("n,R,D", [(5, 300, 128),     # one warp per row, partials in L2
+                                   (24, 32, 128),     # one block per row (a decode's shape)
+                                   (40, 1000, 192),   # one block per row, two lse groups, wide rows
+                                   (20, 64, 512),
+                                   (3, 44000, 128)])  # rows requested before the weights (> 64 MB)
+def test_lse_merge_ignores_rows_of_zero_weight(ca, n, R, D):
+    """A partial whose lse is -inf adds nothing, whatever its o row holds:
+    rows of NaN there must give the oracle's merge of the same partials with
+    those rows zero, online and with a const-max bound."""
+    rng = np.random.default_rng(30 + n)
+    op = rng.standard_normal((n, R, D)).astype(np.float32)
+    lp = (rng.standard_normal((n, R)) * 3).astype(np.float32)
+    lp[0, ::3] = -np.inf
+    lp[n - 1, 1::4] = -np.inf
+    lp[:, 2] = -np.inf  # an all-empty row
+    dead = np.isneginf(lp)
+    clean = np.where(dead[:, :, None], 0.0, op)
+    dirty = np.where(dead[:, :, None], np.float32(np.nan), op).astype(np.float32)
+    ro, rl = oracle.lse_merge(clean, lp)
+    o, lse = ca.lse_merge(torch.tensor(dirty, device="cuda"), torch.tensor(lp, device="cuda"),
+                          out_dtype=torch.float32)
+    assert_close(np32(o), ro, np32(lse), rl, dtype=torch.float32, what=f"merge, NaN rows of weight 0, n={n} R={R}")
+    # const max: unnormalised sums o_i l_i with lse_i = c + ln l_i; rows with
+    # l_i = 0 (lse_i = -inf) hold NaN
+    c = (np.where(dead, -np.inf, lp).max(axis=0) + 1.5).astype(np.float32)
+    c[2] = 0.0
+    l_i = np.exp(lp.astype(np.float64) - c.astype(np.float64))
+    unnorm = np.where(dead[:, :, None], np.float32(np.nan), (op * l_i[:, :, None])).astype(np.float32)
+    live = ~dead.all(axis=0)
+    o, lse = ca.lse_merge(torch.tensor(unnorm, device="cuda"), torch.tensor(lp, device="cuda"),
+                          c=torch.tensor(c, device="cuda"), out_dtype=torch.float32)
+    assert_close(np32(o)[live], ro[live], np32(lse)[live], rl[live], dtype=torch.float32,
+                 what=f"const-max merge, NaN rows of weight 0, n={n} R={R}")
+    assert np.all(np32(o)[~live] == 0.0)  # no partial: the 1e-37 clamp leaves o = 0
+
+
 def test_const_max_bound_kernel(ca):
     from context_attention_gb300 import synth
 
