@@ -508,6 +508,8 @@ ca_status ca_dcp_decode_paged(const void* q, const void* k_cache, const void* v_
       block_size != 128)
     return CA_ERR_UNSUPPORTED;
   if ((int64_t)dcp * nblk * Hkv * block_size >= ((int64_t)1 << 31)) return CA_ERR_UNSUPPORTED;
+  // the slots the block tables address, as the kernel's 32-bit work walk counts them
+  if ((int64_t)dcp * N * Hkv * max_blocks * block_size >= ((int64_t)1 << 31)) return CA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))

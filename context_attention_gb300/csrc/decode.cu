@@ -77,7 +77,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 struct DecParams {
   DecodeArgs a;
   int G;
-  int64_t units;  // pairs * stages
+  uint32_t units;            // pairs * stages, or pairs * splits when dealt (< 2^31)
+  uint32_t range_q, range_r;  // units / ctas, units % ctas
   float scale_log2;
 };
 
@@ -116,32 +117,42 @@ struct Seg {
   bool last;         // the segment ends the pair (its CTA writes the unused slots)
 };
 
-// CTA c deals with units [c * U / C, (c + 1) * U / C); unit x is on CTA
-// ((x + 1) * C - 1) / U, the last c whose range starts at or before x.
-__device__ __forceinline__ int64_t range_begin(int64_t U, int C, int64_t c) { return c * U / C; }
-__device__ __forceinline__ int64_t cta_of_unit(int64_t U, int C, int64_t x) {
-  return ((x + 1) * C - 1) / U;
+// Integer work per segment is 32-bit: a unit, a pair, a slot or a position
+// is below 2^31 (the host rejects caches of 2^31 rows or more), and a 64-bit
+// division costs ~350 cycles; the first segment's nine of them held every
+// CTA's first load back by ~1.5 us.
+//
+// CTA c deals with units [c * U / C, (c + 1) * U / C), computed as
+// c * (U / C) + c * (U % C) / C with the quotient and remainder from the
+// host; unit x is on CTA ((x + 1) * C - 1) / U, the last c whose range
+// starts at or before x.
+__device__ __forceinline__ uint32_t range_begin(const DecParams& P, uint32_t c) {
+  return c * P.range_q + (c * P.range_r) / (uint32_t)P.a.ctas;
+}
+__device__ __forceinline__ uint32_t cta_of_unit(const DecParams& P, uint32_t x) {
+  return (uint32_t)((((uint64_t)x + 1) * (uint64_t)P.a.ctas - 1) / P.units);
 }
 
 // The pair's valid local slots and first cache row of its slot t0.
-__device__ __forceinline__ void pair_of(const DecParams& P, int64_t pair, Seg& S, int64_t* valid) {
+__device__ __forceinline__ void pair_of(const DecParams& P, uint32_t pair, Seg& S, int* valid) {
   const DecodeArgs& a = P.a;
-  S.hkv = (int)(pair % a.Hkv);
-  const int64_t rest = pair / a.Hkv;
-  S.n = (int)(rest % a.N);
-  S.r = (int)(rest / a.N);
-  const int64_t seq = a.seq_lens ? (int64_t)a.seq_lens[S.n] : (int64_t)a.W * a.Lloc;
-  int64_t v = a.ring_layout < 0 ? dcp_local_filled(seq, a.W, a.I, a.I, S.r)
-                                : ring_shard_filled(seq, a.W, a.Lloc, a.ring_layout, S.r);
-  *valid = v > a.Lloc ? a.Lloc : v;
+  S.hkv = (int)(pair % (uint32_t)a.Hkv);
+  const uint32_t rest = pair / (uint32_t)a.Hkv;
+  S.n = (int)(rest % (uint32_t)a.N);
+  S.r = (int)(rest / (uint32_t)a.N);
+  const int Lloc = (int)a.Lloc;
+  const int seq = a.seq_lens ? a.seq_lens[S.n] : a.W * Lloc;
+  const int v = a.ring_layout < 0 ? dcp_local_filled_t<int>(seq, a.W, a.I, a.I, S.r)
+                                  : ring_shard_filled_t<int>(seq, a.W, Lloc, a.ring_layout, S.r);
+  *valid = v > Lloc ? Lloc : v;
 }
 
 // Segment stages [s0, s1) of the pair: tokens [s0 * 128, min(s1 * 128, valid)).
-__device__ __forceinline__ void seg_tokens(const DecParams& P, int64_t s0, int64_t s1, int64_t valid,
+__device__ __forceinline__ void seg_tokens(const DecParams& P, uint32_t s0, uint32_t s1, int valid,
                                            Seg& S) {
   const DecodeArgs& a = P.a;
-  S.t0 = s0 * kTok;
-  const int64_t t1 = s1 * kTok < valid ? s1 * kTok : valid;
+  S.t0 = (int64_t)s0 * kTok;
+  const int64_t t1 = (int64_t)s1 * kTok < valid ? (int64_t)s1 * kTok : valid;
   S.ntok = t1 > S.t0 ? t1 - S.t0 : 0;
   S.row0 = a.ring_layout < 0 ? (((int64_t)S.r * a.N + S.n) * a.Hkv + S.hkv) * a.Lloc + S.t0
                               : (((int64_t)S.n * a.Hkv + S.hkv) * a.W + S.r) * a.Lloc + S.t0;
@@ -150,7 +161,7 @@ __device__ __forceinline__ void seg_tokens(const DecParams& P, int64_t s0, int64
 // Walks one CTA's segments in order; the producer and the consumers each
 // run one and see the same sequence.
 struct SegWalk {
-  int64_t u, u_end;
+  uint32_t u, u_end;
 };
 __device__ __forceinline__ SegWalk seg_walk(const DecParams& P) {
   const DecodeArgs& a = P.a;
@@ -159,33 +170,35 @@ __device__ __forceinline__ SegWalk seg_walk(const DecParams& P) {
     w.u = blockIdx.x;
     w.u_end = P.units;
   } else {
-    w.u = range_begin(P.units, a.ctas, blockIdx.x);
-    w.u_end = range_begin(P.units, a.ctas, blockIdx.x + 1);
+    w.u = range_begin(P, blockIdx.x);
+    w.u_end = range_begin(P, blockIdx.x + 1);
   }
   return w;
 }
 __device__ __forceinline__ bool seg_next(const DecParams& P, SegWalk& w, Seg& S) {
   if (w.u >= w.u_end) return false;
   const DecodeArgs& a = P.a;
-  int64_t valid;
+  int valid;
   if (a.dealt) {
     // unit = (pair, split): a split of split_stages stages, its own slot
-    const int64_t pair = w.u / a.slots, split = w.u % a.slots;
+    const uint32_t slots = (uint32_t)a.slots, ss = (uint32_t)a.split_stages, SP = (uint32_t)a.stages;
+    const uint32_t pair = w.u / slots, split = w.u % slots;
     pair_of(P, pair, S, &valid);
-    const int64_t s0 = split * a.split_stages;
-    const int64_t s1 = s0 + a.split_stages < a.stages ? s0 + a.split_stages : a.stages;
+    const uint32_t s0 = split * ss;
+    const uint32_t s1 = s0 + ss < SP ? s0 + ss : SP;
     seg_tokens(P, s0, s1, valid, S);
     S.slot = (int)split;
     S.last = false;
-    w.u += a.ctas;
+    w.u += (uint32_t)a.ctas;
     return true;
   }
-  const int64_t SP = a.stages;
-  const int64_t pair = w.u / SP, pu0 = pair * SP;
-  const int64_t s1u = w.u_end < pu0 + SP ? w.u_end : pu0 + SP;
+  const uint32_t SP = (uint32_t)a.stages;
+  const uint32_t pair = w.u / SP, pu0 = pair * SP;
+  const uint32_t s1u = w.u_end < pu0 + SP ? w.u_end : pu0 + SP;
   pair_of(P, pair, S, &valid);
   seg_tokens(P, w.u - pu0, s1u - pu0, valid, S);
-  S.slot = (int)(blockIdx.x - cta_of_unit(P.units, a.ctas, pu0));
+  // a pair that starts inside this CTA's range has this CTA as its first
+  S.slot = w.u == pu0 ? 0 : (int)(blockIdx.x - cta_of_unit(P, pu0));
   S.last = s1u == pu0 + SP;
   w.u = s1u;
   return true;
@@ -573,7 +586,11 @@ cudaError_t launch_dcp_decode_partials(const DecodeArgs& a, cudaStream_t stream)
   DecParams P;
   P.a = a;
   P.G = a.Hq / a.Hkv;
-  P.units = (int64_t)a.W * a.N * a.Hkv * (a.dealt ? a.slots : a.stages);
+  const int64_t units = (int64_t)a.W * a.N * a.Hkv * (a.dealt ? a.slots : a.stages);
+  if (units >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;  // the host's row bound keeps it below
+  P.units = (uint32_t)units;
+  P.range_q = a.ctas > 0 ? P.units / (uint32_t)a.ctas : 0;
+  P.range_r = a.ctas > 0 ? P.units % (uint32_t)a.ctas : 0;
   P.scale_log2 = a.scale * kLog2e;
   if (P.units == 0 || a.ctas <= 0) return cudaSuccess;
   CUtensorMap tk, tv;

@@ -72,33 +72,44 @@ CA_HD int64_t dcp_local_to_global(int64_t s, int R, int W, int I) {
   return (s / I) * ((int64_t)W * I) + (int64_t)R * I + s % I;
 }
 
-// local_filled, evaluated as the DCP page prints it.
-CA_HD int64_t dcp_local_filled(int64_t N, int W, int I, int block_size, int R) {
-  const int64_t vblock = (int64_t)block_size * W;
-  const int64_t stride = (int64_t)I * W;
-  const int64_t rank_start = (int64_t)R * I;
-  int64_t filled = (N / vblock) * block_size;
-  const int64_t remaining = N - (N / vblock) * vblock;
+// local_filled, evaluated as the DCP page prints it.  T is the integer type
+// of the arithmetic: int64_t on the host; the decode kernel takes int, whose
+// divisions cost a tenth of 64-bit ones, for its positions are below 2^31
+// (the host rejects caches of 2^31 rows or more).
+template <typename T>
+CA_HD T dcp_local_filled_t(T N, T W, T I, T block_size, T R) {
+  const T vblock = block_size * W;
+  const T stride = I * W;
+  const T rank_start = R * I;
+  T filled = (N / vblock) * block_size;
+  const T remaining = N - (N / vblock) * vblock;
   filled += (remaining / stride) * I;
-  const int64_t leftover = remaining - (remaining / stride) * stride;
-  int64_t extra = leftover - rank_start;
+  const T leftover = remaining - (remaining / stride) * stride;
+  T extra = leftover - rank_start;
   if (extra < 0) extra = 0;
   if (extra > I) extra = I;
   return filled + extra;
 }
+CA_HD int64_t dcp_local_filled(int64_t N, int W, int I, int block_size, int R) {
+  return dcp_local_filled_t<int64_t>(N, W, I, block_size, R);
+}
 
 // Slots of ring-layout shard r (Ls rows) that hold one of the global
 // positions [0, N): contiguous shard r holds [r*Ls, (r+1)*Ls); striped shard
-// r holds r, r + cp, r + 2 cp, ... ("Sharding the Input").
-CA_HD int64_t ring_shard_filled(int64_t N, int cp, int64_t Ls, int layout, int r) {
-  int64_t n;
+// r holds r, r + cp, r + 2 cp, ... ("Sharding the Input").  T as above.
+template <typename T>
+CA_HD T ring_shard_filled_t(T N, T cp, T Ls, int layout, T r) {
+  T n;
   if (layout == kLayoutStriped)
     n = N > r ? (N - r + cp - 1) / cp : 0;
   else
-    n = N - (int64_t)r * Ls;
+    n = N - r * Ls;
   if (n < 0) n = 0;
   if (n > Ls) n = Ls;
   return n;
+}
+CA_HD int64_t ring_shard_filled(int64_t N, int cp, int64_t Ls, int layout, int r) {
+  return ring_shard_filled_t<int64_t>(N, cp, Ls, layout, r);
 }
 
 // dcp_active_mask as the DCP page prints it.

@@ -356,8 +356,10 @@ ca_status ca_ring_decode(const void *q, const void *k, const void *v,
  * seq_lens    device int32 [N] (required; at most dcp*max_blocks*block_size).
  * workspace   ca_dcp_decode_workspace_size(N, Hq, Hkv,
  *             max_blocks*block_size, D, dcp, interleave) bytes.
- * Errors: CA_ERR_UNSUPPORTED unless bf16, D = 128, Hq/Hkv <= 8 and
- * block_size in {8, 16, 32, 64, 128}.
+ * Errors: CA_ERR_UNSUPPORTED unless bf16, D = 128, Hq/Hkv <= 8,
+ * block_size in {8, 16, 32, 64, 128}, and both dcp*nblk*Hkv*block_size (the
+ * caches' rows) and dcp*N*Hkv*max_blocks*block_size (the slots the block
+ * tables address) below 2^31.
  * ---------------------------------------------------------------------- */
 ca_status ca_dcp_decode_paged(const void *q, const void *k_cache,
                               const void *v_cache, const int32_t *block_tables,

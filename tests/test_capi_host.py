@@ -189,6 +189,35 @@ def test_merge_bound_decode_layout_validation(ca):
     assert S[lib.ca_dcp_shard_kv(FAKE, FAKE, 2, 100, 256, 4, 16, None)] == "CA_ERR_SHAPE"
 
 
+def test_paged_decode_validation(ca):
+    """Host checks of the paged decode, none of which reaches the GPU: the
+    caches' rows and the slots the block tables address must each stay
+    below 2^31 (the kernel walks its work in 32-bit integers)."""
+    lib = ca._load()
+    S = ca.STATUS
+
+    def pdec(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, bt=FAKE, dtype=1, N=2, Hq=8, Hkv=2, nblk=64, bs=16, mb=32, D=128, W=4,
+                 I=16, seq=FAKE, scale=0.0, o=FAKE, lse=FAKE, ws=FAKE, ws_bytes=1 << 30, stream=None)
+        a.update(kw)
+        return S[lib.ca_dcp_decode_paged(a["q"], a["k"], a["v"], a["bt"], a["dtype"], a["N"], a["Hq"], a["Hkv"],
+                                         a["nblk"], a["bs"], a["mb"], a["D"], a["W"], a["I"], a["seq"], a["scale"],
+                                         a["o"], a["lse"], a["ws"], a["ws_bytes"], a["stream"])]
+
+    assert pdec(seq=None) == "CA_ERR_INVALID_ARG"       # lengths are required
+    assert pdec(bt=None) == "CA_ERR_INVALID_ARG"
+    assert pdec(Hq=6, Hkv=4) == "CA_ERR_SHAPE"
+    assert pdec(bs=24) == "CA_ERR_UNSUPPORTED"
+    assert pdec(D=64) == "CA_ERR_UNSUPPORTED"
+    assert pdec(nblk=1 << 26) == "CA_ERR_UNSUPPORTED"   # 4 * 2^26 * 2 * 16 cache rows
+    assert pdec(N=1 << 12, mb=1 << 12) == "CA_ERR_UNSUPPORTED"  # 4 * 2^12 * 2 * 2^12 * 16 addressed slots
+    # 2^30 addressed slots pass the size checks; the 16-byte workspace then
+    # stops the call before anything is launched
+    assert pdec(N=1 << 11, mb=1 << 12, ws_bytes=16) == "CA_ERR_WORKSPACE"
+    assert pdec(k=FAKE + 8) == "CA_ERR_ALIGNMENT"
+    assert pdec(ws=None) == "CA_ERR_WORKSPACE"
+
+
 def test_dcp_prefill_validation(ca):
     lib = ca._load()
     S = ca.STATUS
