@@ -68,7 +68,9 @@ cudaError_t launch_const_max_bound(const void* q, const void* k, int is_bf16, in
 // partial and are launched with programmatic stream serialization, so the
 // kernel ahead of them (the decode partials, which release them early) and
 // the merge overlap their launch; after any other kernel the wait is the
-// ordinary stream order.
+// ordinary stream order.  Once past the wait they release the kernel after
+// them, so a following decode, launched the same way, sets up while the
+// merge runs and waits before it touches global memory.
 cudaError_t launch_lse_merge(const float* o_parts, const float* lse_parts, int n,
                              int64_t R, int D, const float* c, void* o, int out_bf16,
                              float* lse, cudaStream_t stream);

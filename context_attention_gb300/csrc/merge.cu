@@ -47,6 +47,7 @@ lse_merge_kernel(const float* __restrict__ o_parts, const float* __restrict__ ls
                  int64_t R, int D, const float* __restrict__ c, void* __restrict__ o, int out_bf16,
                  float* __restrict__ lse) {
   griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x % 32;
   const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + threadIdx.x / 32;
   if (row >= R) return;
@@ -178,6 +179,7 @@ lse_merge_prefetch_kernel(const float* __restrict__ o_parts, const float* __rest
                  int64_t R, int D, const float* __restrict__ c, void* __restrict__ o, int out_bf16,
                  float* __restrict__ lse) {
   griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x % 32;
   const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + threadIdx.x / 32;
   if (row >= R) return;
@@ -284,6 +286,7 @@ lse_merge_wide_kernel(const float* __restrict__ o_parts, const float* __restrict
                       int out_bf16, float* __restrict__ lse) {
   __shared__ float4 red[kWarpsPerBlock][32 * kMaxChunks];
   griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
   const int64_t row = blockIdx.x;
   const int nch = D / 4;  // D % 4 == 0 is checked by the host
