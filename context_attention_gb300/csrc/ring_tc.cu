@@ -207,10 +207,12 @@ struct Step {
   int rank;       // kMaskDcp: rank whose current tokens these are
 };
 
+// kSegMode 0: the ring schedule only; 1: the segmented schedule when P.seg.
+template <int kSegMode>
 __device__ __forceinline__ Step step_info(const TcParams& P, const Unit& U, int t) {
   Step st;
   const int64_t a_max = min(U.qrow0 + P.unit_rows - 1, P.a.Ls - 1);
-  if (P.seg) {
+  if (kSegMode != 0 && P.seg) {
     const int R = P.part_rank >= 0 ? P.part_rank : (t >> 1);
     st.rank = R;
     st.row0 = 0;
@@ -249,31 +251,34 @@ __device__ __forceinline__ Step step_info(const TcParams& P, const Unit& U, int 
   return st;
 }
 
+template <int kSegMode>
 __device__ __forceinline__ int unit_tiles(const TcParams& P, const Unit& U) {
   int n = 0;
-  for (int t = 0; t < P.nsteps; ++t) n += step_info(P, U, t).nk;
+  for (int t = 0; t < P.nsteps; ++t) n += step_info<kSegMode>(P, U, t).nk;
   return n;
 }
 
 // Last key of step `st` visible to query row a (may be < 0: none).
+template <int kSegMode>
 __device__ __forceinline__ int64_t step_row_limit(const TcParams& P, const Step& st, int64_t a) {
   int64_t lim = st.nkeys - 1;
   if (st.mask == kMaskDelta) {
     lim = min(lim, a - st.delta);
-  } else if (st.mask == kMaskDcp) {
+  } else if (kSegMode != 0 && st.mask == kMaskDcp) {
     lim = min(lim, dcp_local_filled(a + 1, P.W, P.I, P.I, st.rank) - 1);
   }
   return lim;
 }
 
 // Walks the (step, key tile) sequence of a unit in order.
+template <int kSegMode>
 struct TileIter {
   int t, kt;
   bool new_step;  // true on the first tile of a step
   Step st;
   __device__ __forceinline__ void seek(const TcParams& P, const Unit& U) {
     while (t < P.nsteps) {
-      st = step_info(P, U, t);
+      st = step_info<kSegMode>(P, U, t);
       if (st.nk > 0) return;
       ++t;
     }
@@ -691,7 +696,11 @@ __device__ __noinline__ void rescale_o_row(uint32_t tO, float f) {
 // 128-key tiles), which then run without the masked softmax's code: on the
 // DiT workload 3.353 -> 3.274 ms, online max 10.93 -> 10.41 ms, bit for bit
 // the same output (the kernel is sensitive to the size of its hot code).
-template <bool kConst, bool kMaskable>
+// kSegMode: 0 compiles the segmented schedule's branches out (the unmasked
+// instantiations; online max 10.37 -> 10.12 ms), 1 decides them by P.seg.
+// Compiling them out of the masked instantiations as well, with a third one
+// for the segmented schedule, made causal and DCP prefill ~1 % slower.
+template <bool kConst, bool kMaskable, int kSegMode>
 __global__ void __launch_bounds__(kThreads, 1)
 ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -758,7 +767,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         const int krow = (int)(st.row0 + (int64_t)kt * kBN);
         for (int hx = 0; hx < 2; ++hx) {
           const uint32_t dst = sbase + kSmemKV + slot * kTileBytes + hx * kBoxBytes;
-          if (P.seg)
+          if (kSegMode != 0 && P.seg)
             tma_load_3d(dst, m, fb, hx * 64, krow, (int)kvh_of);
           else
             tma_load_2d(dst, m, fb, hx * 64, krow);
@@ -769,12 +778,12 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
       // free, so an armed barrier always completes.
       for (int64_t k = 0, u = unit_at(P, 0); u < P.units && ok; ++k, u = unit_at(P, k)) {
         const Unit U = unit_of(P, u);
-        const int n = unit_tiles(P, U);
+        const int n = unit_tiles<kSegMode>(P, U);
         if (n == 0) continue;
         kvh_of = U.bhk;
         ok = mbar_wait(bar(kBarQEmpty), (uc & 1) ^ 1, abort_flag, err) && slot_free(0);
         if (!ok) break;
-        TileIter it;
+        TileIter<kSegMode> it;
         it.begin(P, U);
         // Q tiles and K_0 on q_full
         mbar_arrive_expect_tx(bar(kBarQFull), 3 * kTileBytes);
@@ -837,7 +846,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
                      tO1 = tmem + kColO + 128;
       for (int64_t k = 0, u = unit_at(P, 0); u < P.units && ok; ++k, u = unit_at(P, k)) {
         const Unit U = unit_of(P, u);
-        const int n = unit_tiles(P, U);
+        const int n = unit_tiles<kSegMode>(P, U);
         if (n == 0) continue;
         // Q tiles and K_0
         ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarQFull), uc & 1, abort_flag, err));
@@ -914,7 +923,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
     bool ok = true;
     for (int64_t k = 0, u = unit_at(P, 0); u < P.units && ok; ++k, u = unit_at(P, k)) {
       const Unit U = unit_of(P, u);
-      const int n = unit_tiles(P, U);
+      const int n = unit_tiles<kSegMode>(P, U);
       const int64_t a_row = tile_row0(P, U, i) + tid;
       const bool valid = a_row < P.a.Ls;
       const int64_t orow = tile_bh(U, i) * P.a.Sq + (int64_t)U.r_store * P.a.Ls + a_row;
@@ -967,7 +976,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
       int pend = 0;         // reference move (log2 units) due before the next tile
       float l = 0.f;   // row sum of p as computed (log-sum-exp)
       float lr = 0.f;  // row sum of p rounded to bf16 (normalisation)
-      TileIter it;
+      TileIter<kSegMode> it;
       it.begin(P, U);
       int64_t row_lim = 0;
       for (int j = 0; j < n; ++j) {
@@ -982,7 +991,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
           if (j == n - 1) mbar_arrive(bar(kBarQEmpty));
         }
         // last visible column of this tile for this row
-        if (it.new_step) row_lim = step_row_limit(P, it.st, a_row);
+        if (it.new_step) row_lim = step_row_limit<kSegMode>(P, it.st, a_row);
         const int64_t lim = row_lim - (int64_t)it.kt * kBN;
         const int vis_max = (int)max((int64_t)-1, min(lim, (int64_t)(kBN - 1)));
         const bool need_mask = kMaskable && __any_sync(0xffffffffu, vis_max < kBN - 1);
@@ -1168,20 +1177,20 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
 
 }  // namespace
 
-template <bool kConst, bool kMaskable>
+template <bool kConst, bool kMaskable, int kSegMode>
 static cudaError_t launch_tc_mode(const TcMaps& maps, const TcParams& P, cudaStream_t stream) {
   static std::atomic<int> attr_set[64];  // idempotent once-per-device setup
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(ring_tc_kernel<kConst, kMaskable>,
+    cudaError_t e = cudaFuncSetAttribute(ring_tc_kernel<kConst, kMaskable, kSegMode>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
   const int sms = device_sm_count();
   const int64_t grid = P.units < sms ? P.units : sms;
-  ring_tc_kernel<kConst, kMaskable><<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(maps, P);
+  ring_tc_kernel<kConst, kMaskable, kSegMode><<<(unsigned)grid, kThreads, kSmemAlloc, stream>>>(maps, P);
   return cudaGetLastError();
 }
 
@@ -1191,8 +1200,10 @@ static cudaError_t launch_tc_mode(const TcMaps& maps, const TcParams& P, cudaStr
 static cudaError_t launch_tc(const TcMaps& maps, const TcParams& P, cudaStream_t stream) {
   const bool maskable = P.a.causal || P.seg || P.a.Ls % kBN != 0;
   if (P.a.mode == 1)
-    return maskable ? launch_tc_mode<true, true>(maps, P, stream) : launch_tc_mode<true, false>(maps, P, stream);
-  return maskable ? launch_tc_mode<false, true>(maps, P, stream) : launch_tc_mode<false, false>(maps, P, stream);
+    return maskable ? launch_tc_mode<true, true, 1>(maps, P, stream)
+                    : launch_tc_mode<true, false, 0>(maps, P, stream);
+  return maskable ? launch_tc_mode<false, true, 1>(maps, P, stream)
+                  : launch_tc_mode<false, false, 0>(maps, P, stream);
 }
 
 static void init_common(TcParams& P, const RingArgs& a) {
