@@ -488,16 +488,19 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 
 // The two row sums of a softmax row.  `l` sums p as computed (fp32): it gives
 // the log-sum-exp.  `lr` is the sum O is divided by.  On a tile that needs a
-// mask (a causal diagonal, a shard's ragged end) lr sums p as the PV product
-// consumes it, rounded to bf16, so that every weight in the numerator is
-// matched by the same weight in the denominator ("Accumulate, then normalize
-// once": the accumulator and its row sum come from one set of weights): the
-// rows that see only a handful of keys -- where one weight's rounding error
-// would otherwise move o by up to 2^-8 |o| -- get o as an exact convex
-// combination of their V rows up to fp32 accumulation.  On unmasked tiles lr
-// takes the fp32 p like l: there a row's weight is spread over whole tiles
-// of keys, and forming the rounded sum on every tile costs 8-14 % of the
-// kernel's throughput (the softmax warps' issue slots are the bound).
+// mask (a causal diagonal, a shard's ragged end), for a warp holding a row
+// that sees fewer than kRoundedSumKeys keys in all, lr sums p as the PV
+// product consumes it, rounded to bf16, so that every weight in the
+// numerator is matched by the same weight in the denominator ("Accumulate,
+// then normalize once": the accumulator and its row sum come from one set of
+// weights): the rows that see only a handful of keys -- where one weight's
+// rounding error would otherwise move o by up to 2^-8 |o| -- get o as an
+// exact convex combination of their V rows up to fp32 accumulation.
+// Elsewhere lr takes the fp32 p like l: there a row's weight is spread over
+// a thousand keys or more, and forming the rounded sum on every tile costs
+// 8-14 % of the kernel's throughput (the softmax warps' issue slots are the
+// bound); on the masked tiles of many-key rows it cost striped causal 0.75 %.
+constexpr int64_t kRoundedSumKeys = 1024;
 
 struct RowSums {
   uint64_t l2, lr2;  // packed pairs of partial sums
@@ -543,12 +546,12 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&r)[32], int ch, int v
 }
 
 // A tile's (l, lr): on an unmasked tile lr is l itself.
-template <bool kMask>
+template <bool kInl>
 __device__ __forceinline__ float2 tile_sums(const RowSums& rs) {
   float lo, hi;
   f2_unpack(rs.l2, lo, hi);
   const float l = lo + hi;
-  if (!kMask) return make_float2(l, l);
+  if (!kInl) return make_float2(l, l);
   f2_unpack(rs.lr2, lo, hi);
   return make_float2(l, lo + hi);
 }
@@ -614,12 +617,12 @@ __device__ __forceinline__ void exp_chunk_masked(const uint32_t (&r)[32], int ch
 }
 
 // The chunk of a masked tile (kMask) or of an unmasked one.
-template <bool kMask>
+template <bool kMask, bool kInl>
 __device__ __forceinline__ void exp_chunk_any(const uint32_t (&r)[32], int ch, int vis_max,
                                               uint64_t sl2_2, uint64_t nref_2, RowSums& rs,
                                               uint32_t tS) {
   if (kMask)
-    exp_chunk_masked<true>(r, ch, vis_max, sl2_2, nref_2, rs, tS);
+    exp_chunk_masked<kInl>(r, ch, vis_max, sl2_2, nref_2, rs, tS);
   else
     exp_chunk<false, false>(r, ch, vis_max, sl2_2, nref_2, rs, tS);
 }
@@ -628,7 +631,7 @@ __device__ __forceinline__ void exp_chunk_any(const uint32_t (&r)[32], int ch, i
 // next 32-column load in flight while the current chunk is processed.  P
 // block ch overwrites S columns [16ch, 16ch+16), which were already read.
 // Returns the tile's (l, lr) sums.
-template <bool kMask>
+template <bool kMask, bool kInl = kMask>
 __device__ __forceinline__ float2 exp_row_to_tmem(uint32_t tS, int vis_max, float sl2, float ref) {
   uint32_t ra[32], rb[32];
   const uint64_t sl2_2 = f2_pack(sl2, sl2), nref_2 = f2_pack(-ref, -ref);
@@ -637,19 +640,19 @@ __device__ __forceinline__ float2 exp_row_to_tmem(uint32_t tS, int vis_max, floa
   tmem_ld_wait();
   reg_fence(ra);
   tmem_ld32(tS + 32, rb);
-  exp_chunk_any<kMask>(ra, 0, vis_max, sl2_2, nref_2, rs, tS);
+  exp_chunk_any<kMask, kInl>(ra, 0, vis_max, sl2_2, nref_2, rs, tS);
   tmem_ld_wait();
   reg_fence(rb);
   tmem_ld32(tS + 64, ra);
-  exp_chunk_any<kMask>(rb, 1, vis_max, sl2_2, nref_2, rs, tS);
+  exp_chunk_any<kMask, kInl>(rb, 1, vis_max, sl2_2, nref_2, rs, tS);
   tmem_ld_wait();
   reg_fence(ra);
   tmem_ld32(tS + 96, rb);
-  exp_chunk_any<kMask>(ra, 2, vis_max, sl2_2, nref_2, rs, tS);
+  exp_chunk_any<kMask, kInl>(ra, 2, vis_max, sl2_2, nref_2, rs, tS);
   tmem_ld_wait();
   reg_fence(rb);
-  exp_chunk_any<kMask>(rb, 3, vis_max, sl2_2, nref_2, rs, tS);
-  return tile_sums<kMask>(rs);
+  exp_chunk_any<kMask, kInl>(rb, 3, vis_max, sl2_2, nref_2, rs, tS);
+  return tile_sums<kInl>(rs);
 }
 
 // O *= f for this thread's row, out of line: the deferred reference move of
@@ -679,7 +682,11 @@ __device__ __noinline__ float row_max_masked(uint32_t tS, int vis_max) {
   return row_max_from_tmem<true>(tS, vis_max);
 }
 __device__ __noinline__ float2 exp_row_masked(uint32_t tS, int vis_max, float sl2, float ref) {
-  return exp_row_to_tmem<true>(tS, vis_max, sl2, ref);
+  return exp_row_to_tmem<true, true>(tS, vis_max, sl2, ref);
+}
+// The same without the rounded row sum, for rows that see many keys in all.
+__device__ __noinline__ float2 exp_row_masked_plain(uint32_t tS, int vis_max, float sl2, float ref) {
+  return exp_row_to_tmem<true, false>(tS, vis_max, sl2, ref);
 }
 
 // kConst: the const-max instantiation (no running maximum) or the online-max
@@ -932,6 +939,15 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         }
         continue;
       }
+      // Rows that see few keys in all form the rounded sum on their masked
+      // tiles (causal ring: a row sees its global position + 1 keys, else
+      // all of them; the segmented and single-step schedules always do)
+      bool few_keys = true;
+      if (kMaskable && !P.seg && P.a.kv_rank_fixed < 0) {
+        const int64_t keys = P.a.causal ? layout_global(P.a.layout, P.a.cp, P.a.Ls, U.r_log, a_row) + 1
+                                        : (int64_t)P.a.cp * P.a.Ls;
+        few_keys = __any_sync(0xffffffffu, valid && keys < kRoundedSumKeys);
+      }
       float c_nat = 0.f;
       if (const_max && P.a.kmax2) {
         // the row's bound from its q row in the Q tile: |q|^2 summed in fp32
@@ -1060,7 +1076,8 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         // pass 2: p = 2^(s*scale*log2e - ref), row sum, bf16 P written over
         // the S columns already consumed (P column block ch < S block ch+1)
         if (!p_done) {
-          const float2 t = need_mask ? exp_row_masked(tS, vis_max, P.scale_log2, mref)
+          const float2 t = need_mask ? (few_keys ? exp_row_masked(tS, vis_max, P.scale_log2, mref)
+                                                 : exp_row_masked_plain(tS, vis_max, P.scale_log2, mref))
                                      : exp_row_to_tmem<false>(tS, vis_max, P.scale_log2, mref);
           tl = t.x;
           tlr = t.y;
