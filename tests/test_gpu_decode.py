@@ -111,6 +111,34 @@ def test_decode_one_sequence_131k(ca):
     assert_close(np32(o), ro, np32(lse), rl, what="decode, one sequence of 100001 tokens")
 
 
+@pytest.mark.parametrize("N", [1, 8])
+def test_back_to_back_decodes_share_a_workspace(ca, N):
+    """Decodes queued back to back on one stream with one workspace: each is
+    launched as a programmatic dependent and sets up while the previous
+    call's merge still reads that workspace, so it must touch no global
+    memory before its grid dependency resolves.  Every output must equal the
+    same call made alone (one sequence: contiguous CTA ranges and the
+    one-block-per-row merge; eight: dealt splits)."""
+    from context_attention_gb300 import synth
+
+    Hq, Hkv, W, I, Lloc = 32, 8, 4, 16, 4096
+    q, k, v = synth.decode_inputs(N, Hq, Hkv, 128, W, Lloc, 80 + N, device="cuda")
+    qs = [q] + [torch.randn_like(q.float()).to(q.dtype) for _ in range(3)]
+    ws = torch.empty(ca.dcp_decode_workspace_size(N, Hq, Hkv, Lloc, 128, W, I), dtype=torch.uint8, device="cuda")
+    alone = []
+    for qq in qs:
+        o, lse = ca.dcp_decode(qq, k, v, I, workspace=ws)
+        torch.cuda.synchronize()
+        alone.append((o.clone(), lse.clone()))
+    outs = [(torch.empty_like(q), torch.empty(N, Hq, device="cuda")) for _ in qs]
+    for _ in range(3):
+        for qq, (o, lse) in zip(qs, outs):
+            ca.dcp_decode(qq, k, v, I, out=o, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    for (o, lse), (oa, la) in zip(outs, alone):
+        assert torch.equal(o, oa) and torch.equal(lse, la)
+
+
 def test_decode_zero_length_sequence(ca):
     """seq_len = 0: every partial is empty: o = 0, lse = -inf."""
     from context_attention_gb300 import synth
