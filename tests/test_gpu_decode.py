@@ -139,6 +139,26 @@ def test_back_to_back_decodes_share_a_workspace(ca, N):
         assert torch.equal(o, oa) and torch.equal(lse, la)
 
 
+def test_decode_single_pair_many_partials(ca):
+    """One shard, one sequence, one KV head (eight query heads): the single
+    pair's 1024 stages are cut over every CTA, so each row merges one partial
+    per CTA (about 150, beyond the merge's groups of 32); lengths full and
+    ending mid-stage, NaN past the valid slots."""
+    from context_attention_gb300 import synth
+
+    N, Hq, Hkv, W, I, Lloc = 1, 8, 1, 1, 16, 131072
+    q, k, v = synth.decode_inputs(N, Hq, Hkv, 128, W, Lloc, 90, device="cuda")
+    for L in (Lloc, 100001):
+        kk, vv = k.clone(), v.clone()
+        kk[0, 0, :, L:] = float("nan")
+        vv[0, 0, :, L:] = float("nan")
+        sl = torch.tensor([L], dtype=torch.int32, device="cuda")
+        o, lse = ca.dcp_decode(q, kk, vv, I, seq_lens=sl)
+        ro, rl = oracle.dcp_decode(np32(q), np32(torch.nan_to_num(kk)), np32(torch.nan_to_num(vv)), I,
+                                   seq_lens=[L])
+        assert_close(np32(o), ro, np32(lse), rl, what=f"decode, one pair, L={L}")
+
+
 def test_decode_zero_length_sequence(ca):
     """seq_len = 0: every partial is empty: o = 0, lse = -inf."""
     from context_attention_gb300 import synth
