@@ -678,11 +678,28 @@ def causal_rank_imbalance(S, cp, layout):
     return round(max(work) / (sum(work) / cp), 4)
 
 
-def bench_other_workloads(ca, torch, reps=5, cpu_seconds=None):
+def median_launch_ms(torch, stream, launch, reps):
+    """Median of `reps` individually timed launches: CUDA events on the
+    launching stream around each, the launches back to back."""
+    evs = []
+    for i in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        launch(i)
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def bench_other_workloads(ca, torch, reps=10, cpu_seconds=None):
     """Device time of the other workloads (online max, sink keys, causal GQA
     in both layouts, the QKV prologue, DCP prefill, paged and Ring Pass-Q
-    decode, DCP decode of one and two sequences) with the same CUDA-event
-    method; each is reported with its algorithmic rate (causal counts
+    decode, DCP decode of one and two sequences): the median of `reps`
+    individually timed launches (CUDA events), after 3 warm-ups; the one- and
+    two-sequence decodes are 10 * reps launches back to back under one pair
+    of events.  Each is reported with its algorithmic rate (causal counts
     visible pairs).  With cpu_seconds, each also gets the oracle timed on a
     sample of about that many seconds."""
     from context_attention_gb300 import synth
@@ -698,14 +715,9 @@ def bench_other_workloads(ca, torch, reps=5, cpu_seconds=None):
                          device="cuda")
         for _ in range(3):
             ca.ring_attn_fwd(q, k, v, cp, mode=mode, causal=causal, layout=layout, out=out, lse=lse, workspace=ws)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            ca.ring_attn_fwd(q, k, v, cp, mode=mode, causal=causal, layout=layout, out=out, lse=lse, workspace=ws)
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / reps
+        ms = median_launch_ms(torch, stream, lambda i: ca.ring_attn_fwd(q, k, v, cp, mode=mode, causal=causal,
+                                                                      layout=layout, out=out, lse=lse,
+                                                                      workspace=ws), reps)
         res[name] = {"ms": round(ms, 3), "tflops": round(flops / (ms / 1e3) / 1e12, 1)}
         if cpu_seconds:
             res[name]["cpu_baseline"] = oracle_ring_baseline(q, k, v, cp, mode, causal, layout, cpu_seconds,
@@ -736,19 +748,15 @@ def bench_other_workloads(ca, torch, reps=5, cpu_seconds=None):
     torch.cuda.synchronize()
     outs = [ca.qkv_prologue(x_q, x_k, H, H, x_v=x_v, g_q=g_q, g_k=g_k, rope_cos=cos, rope_sin=sin, cp_size=8)
             for _ in range(2)]  # two output sets (> L2 together) so no rep reads the previous one's lines
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for i in range(4 * reps):
+    def prologue_launch(i):
         o = outs[i % 2]
         st = ca._load().ca_qkv_prologue(x_q.data_ptr(), x_k.data_ptr(), x_v.data_ptr(), g_q.data_ptr(),
                                         g_k.data_ptr(), 1e-6, cos.data_ptr(), sin.data_ptr(), 1, B, S, H, H, D, 8, 0,
                                         o[0].data_ptr(), o[1].data_ptr(), o[2].data_ptr(), o[3].data_ptr(),
                                         stream.cuda_stream)
         assert st == 0, st
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / (4 * reps)
+
+    ms = median_launch_ms(torch, stream, prologue_launch, 2 * reps)
     nbytes = 6 * B * S * H * D * 2 + 2 * S * (D // 2) * 4
     res["qkv_prologue DiT B1 S16384 H40"] = {"ms": round(ms, 4), "gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
     if cpu_seconds:
@@ -763,14 +771,7 @@ def bench_other_workloads(ca, torch, reps=5, cpu_seconds=None):
     lse = torch.empty(Hq, Sc, device="cuda", dtype=torch.float32)
     for _ in range(3):
         ca.dcp_prefill(q, kp, vp, kc, vc, I, P, out=out, lse=lse)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(reps):
-        ca.dcp_prefill(q, kp, vp, kc, vc, I, P, out=out, lse=lse)
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / reps
+    ms = median_launch_ms(torch, stream, lambda i: ca.dcp_prefill(q, kp, vp, kc, vc, I, P, out=out, lse=lse), reps)
     f = 4.0 * 128 * Hq * (Sc * P + Sc * (Sc + 1) / 2)
     res["dcp_prefill Hq32 Hkv8 chunk8192 prior122880 dcp4"] = {"ms": round(ms, 3),
                                                                "tflops": round(f / (ms / 1e3) / 1e12, 1)}
@@ -802,12 +803,8 @@ def bench_other_workloads(ca, torch, reps=5, cpu_seconds=None):
                      dtype=torch.uint8, device="cuda")
     for _ in range(3):
         ca.dcp_decode_paged(q, kc, vc, bt, d["I"], sl, out=out, lse=lse, workspace=ws)
-    a.record(stream)
-    for _ in range(reps):
-        ca.dcp_decode_paged(q, kc, vc, bt, d["I"], sl, out=out, lse=lse, workspace=ws)
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / reps
+    ms = median_launch_ms(torch, stream, lambda i: ca.dcp_decode_paged(q, kc, vc, bt, d["I"], sl, out=out, lse=lse,
+                                                                     workspace=ws), reps)
     res["dcp_decode_paged bs16 64seqs L131072 dcp4"] = {"ms": round(ms, 3),
                                                         "gbs": round(decode_bytes() / (ms / 1e3) / 1e9, 1)}
     if cpu_seconds:
@@ -828,12 +825,8 @@ def bench_other_workloads(ca, torch, reps=5, cpu_seconds=None):
                      device="cuda")
     for _ in range(3):
         ca.ring_decode(q, kr, vr, 8, layout="striped", out=out, lse=lse, workspace=ws)
-    a.record(stream)
-    for _ in range(reps):
-        ca.ring_decode(q, kr, vr, 8, layout="striped", out=out, lse=lse, workspace=ws)
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / reps
+    ms = median_launch_ms(torch, stream, lambda i: ca.ring_decode(q, kr, vr, 8, layout="striped", out=out, lse=lse,
+                                                                workspace=ws), reps)
     res["ring_decode striped cp8 64seqs L131072"] = {"ms": round(ms, 3),
                                                      "gbs": round(decode_bytes() / (ms / 1e3) / 1e9, 1)}
     if cpu_seconds:
@@ -852,7 +845,12 @@ def bench_other_workloads(ca, torch, reps=5, cpu_seconds=None):
                          dtype=torch.uint8, device="cuda")
         for _ in range(3):
             ca.dcp_decode(q, kd, vd, d["I"], out=out, lse=lse, workspace=ws)
-        n_launch = 20 * reps
+        # one pair of events around all launches: an event between two of
+        # them would cut the programmatic dependency that lets each decode
+        # set up while the previous one's merge runs
+        n_launch = 10 * reps
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(n_launch):
             ca.dcp_decode(q, kd, vd, d["I"], out=out, lse=lse, workspace=ws)
