@@ -33,6 +33,7 @@ aggregate over ranks with the max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -92,9 +93,12 @@ LOW_CLOCK_FRACTION = 0.85
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms from before
+    the timed region to after it; the summary keeps the samples taken inside
+    the region (by host time), or all of them when the region is shorter than
+    the sampling interval."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -102,6 +106,7 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = None
+        self.t_in = self.t_out = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -109,13 +114,16 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+                 "-lms", "50", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         time.sleep(0.3)
+        self.t_in = time.time()
         return self
 
     def __exit__(self, *exc):
+        self.t_out = time.time()
+        time.sleep(0.06)  # one more sample after the region
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -126,28 +134,36 @@ class ClockSampler:
     def summary(self):
         if not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sms, maxs, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []  # (host time or None, sm MHz, max MHz, active reasons)
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sms.append(float(parts[1]))
-                    maxs.append(float(parts[2]))
+                    sm, top = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
+                try:
+                    t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    t = None
+                rows.append((t, sm, top, {n for n, v in zip(names, parts[6:10]) if v.lower() == "active"}))
         os.unlink(self.path)
-        if not sms:
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        med, top = statistics.median(sms), max(maxs)
+        inside = [r for r in rows if r[0] is not None and self.t_in is not None and self.t_out is not None
+                  and self.t_in <= r[0] <= self.t_out]
+        window = "inside the timed region" if inside else "around the timed region (shorter than 50 ms)"
+        use = inside or rows
+        sms = [r[1] for r in use]
+        med, top = statistics.median(sms), max(r[2] for r in use)
+        reasons = set().union(*[r[3] for r in use])
         if med < LOW_CLOCK_FRACTION * top and not reasons:
             reasons.add("sm_clock_low_no_reason")  # what a clock lock left behind looks like
-        return {"sm_mhz": med, "sm_max_mhz": top, "samples": len(sms), "reasons": sorted(reasons)}
+        return {"sm_mhz": med, "sm_max_mhz": top, "sm_mhz_min": min(sms), "samples": len(sms),
+                "samples_from": window, "reasons": sorted(reasons)}
 
 
 # a rank that dies leaves the others at their next collective; they give up

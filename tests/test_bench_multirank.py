@@ -178,14 +178,24 @@ def test_input_digest_covers_the_first_mib_of_raw_bytes():
 
 def test_clock_summary_from_sampled_lines(tmp_path):
     """The clock record of a timed region, from nvidia-smi's CSV lines (no
-    header, no units): median and maximum SM clock, the throttle reasons seen
-    active, unparsable lines skipped, and a clock far below its maximum with
-    no reason flagged as a leftover lock (which the bench re-measures)."""
+    header, no units, a timestamp first): median and maximum SM clock, the
+    throttle reasons seen active, unparsable lines skipped, a clock far below
+    its maximum with no reason flagged as a leftover lock (which the bench
+    re-measures), and only the samples taken inside the region kept when
+    there are any."""
+    import datetime
+
     import bench
 
-    def summary(lines):
+    t0 = 1.8e9  # host time the region starts
+
+    def stamp(dt):
+        return datetime.datetime.fromtimestamp(t0 + dt).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+
+    def summary(lines, window=(0.0, 10.0)):
         c = bench.ClockSampler(0)
         c.path = str(tmp_path / "clk.csv")
+        c.t_in, c.t_out = t0 + window[0], t0 + window[1]
         with open(c.path, "w") as f:
             f.write("".join(line + "\n" for line in lines))
         out = c.summary()
@@ -193,10 +203,15 @@ def test_clock_summary_from_sampled_lines(tmp_path):
         return out
 
     na, act = "Not Active", "Active"
-    row = lambda sm, *r: ", ".join(["0", str(sm), "2070", "850.00", "0x0"] + list(r))  # noqa: E731
+
+    def row(sm, *r, dt=1.0):
+        return ", ".join([stamp(dt), "0", str(sm), "2070", "850.00", "0x0"] + list(r))
+
     s = summary([row(1935, na, na, na, act), row(1950, na, na, na, act), row(1700, na, na, na, na),
-                 "0, [N/A], 2070, 1.0, 0x0, Not Active, Not Active, Not Active, Not Active", "garbage"])
-    assert s == {"sm_mhz": 1935.0, "sm_max_mhz": 2070.0, "samples": 3, "reasons": ["sw_power_cap"]}
+                 stamp(1.0) + ", 0, [N/A], 2070, 1.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+                 "garbage"])
+    assert s == {"sm_mhz": 1935.0, "sm_max_mhz": 2070.0, "sm_mhz_min": 1700.0, "samples": 3,
+                 "samples_from": "inside the timed region", "reasons": ["sw_power_cap"]}
     s = summary([row(2070, na, act, na, na), row(2070, na, na, na, na)])
     assert s["reasons"] == ["hw_thermal_slowdown"] and s["sm_mhz"] == 2070.0
     # power-capped low clocks are kept; low clocks with no reason are a lock
@@ -206,6 +221,14 @@ def test_clock_summary_from_sampled_lines(tmp_path):
     assert "sm_clock_low_no_reason" in bench.REJECTED_REASONS
     assert summary([row(1800, na, na, na, na)] * 3)["reasons"] == []  # 0.87 of max: not "well below"
     assert summary([])["reasons"] == ["unsampled"]
+    # idle samples before and after the region do not enter its record ...
+    lines = [row(2070, na, na, na, na, dt=-0.2), row(1700, na, na, na, act, dt=0.02),
+             row(1720, na, na, na, act, dt=0.07), row(2070, na, na, na, na, dt=0.15)]
+    s = summary(lines, window=(0.0, 0.1))
+    assert (s["sm_mhz"], s["samples"], s["reasons"]) == (1710.0, 2, ["sw_power_cap"])
+    # ... unless the region is too short to hold a sample: then all of them do
+    s = summary(lines, window=(0.03, 0.06))
+    assert s["samples"] == 4 and s["samples_from"].startswith("around")
 
 
 def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
