@@ -902,6 +902,13 @@ def run_profile_case(args):
         km = ca.key_max2(k)
         for _ in range(args.warmup + 1):
             ca.ring_attn_fwd_kmax(q, k, v, km, PREFILL["cp"])
+    elif args.profile in ("causal_contiguous", "causal_striped"):
+        # the causal GQA workload itself (B1 Hq32 Hkv8 S65536 D128, cp8, online
+        # max): q,k,v 805 MB (> L2), one launch ~22 ms
+        q, k, v = synth.normal_qkv(1, 32, 8, 65536, 128, 4, dtype=torch.bfloat16, device="cuda")
+        layout = args.profile.split("_")[1]
+        for _ in range(args.warmup + 1):
+            ca.ring_attn_fwd(q, k, v, 8, mode="online_max", causal=True, layout=layout)
     elif args.profile == "prologue":
         # the DiT prologue (B1 S16384 40 heads): 1 GB moved per launch (> L2), ~0.2 ms
         B, S, H, D = 1, PREFILL["S"], PREFILL["H"], PREFILL["D"]
@@ -1135,8 +1142,8 @@ def main():
                     help="oracle seconds of the headline workload's CPU baseline")
     ap.add_argument("--cpu-seconds-each", type=float, default=3.0,
                     help="oracle seconds of each other workload's CPU baseline (decode and other_workloads)")
-    ap.add_argument("--profile", choices=["ring", "decode", "decode_small", "prologue", "key_pass", "merge", "paged",
-                                          "ring_decode"],
+    ap.add_argument("--profile", choices=["ring", "causal_contiguous", "causal_striped", "decode", "decode_small",
+                                          "prologue", "key_pass", "merge", "paged", "ring_decode"],
                     default=None,
                     help="run one small launch of one kernel (for ncu captures) and exit")
     args = ap.parse_args()
