@@ -270,29 +270,56 @@ __device__ __forceinline__ int64_t step_row_limit(const TcParams& P, const Step&
   return lim;
 }
 
-// Walks the (step, key tile) sequence of a unit in order.
-template <int kSegMode>
+// Walks the (step, key tile) sequence of a unit.  kPhased: first the tiles
+// that every row of the unit sees whole, step by step, then, step by step,
+// the rest (a row's last visible key grows with the row, so those are the
+// tail of each step's range, found from the unit's first row): the softmax
+// runs the two phases in separate loops, the first without the masked code.
+template <int kSegMode, bool kPhased>
 struct TileIter {
-  int t, kt;
-  bool new_step;  // true on the first tile of a step
+  int t, kt, kend;
+  int phase;
+  bool new_step;  // true on the first tile of a step within a phase
   Step st;
   __device__ __forceinline__ void seek(const TcParams& P, const Unit& U) {
-    while (t < P.nsteps) {
-      st = step_info<kSegMode>(P, U, t);
-      if (st.nk > 0) return;
-      ++t;
+    if constexpr (!kPhased) {
+      kt = 0;
+      while (t < P.nsteps) {
+        st = step_info<kSegMode>(P, U, t);
+        if (st.nk > 0) return;
+        ++t;
+      }
+    } else {
+      for (;;) {
+        if (t >= P.nsteps) {
+          if (phase == 1) return;
+          phase = 1;
+          t = 0;
+        }
+        st = step_info<kSegMode>(P, U, t);
+        if (st.nk > 0) {
+          const int64_t lo = step_row_limit<kSegMode>(P, st, U.qrow0);
+          const int km = lo < 0 ? 0 : (int)min((int64_t)st.nk, (lo + 1) / kBN);
+          const int k0 = phase == 0 ? 0 : km, k1 = phase == 0 ? km : st.nk;
+          if (k0 < k1) {
+            kt = k0;
+            kend = k1;
+            return;
+          }
+        }
+        ++t;
+      }
     }
   }
   __device__ __forceinline__ void begin(const TcParams& P, const Unit& U) {
     t = 0;
-    kt = 0;
+    phase = 0;
     new_step = true;
     seek(P, U);
   }
   __device__ __forceinline__ void next(const TcParams& P, const Unit& U) {
     new_step = false;
-    if (++kt < st.nk) return;
-    kt = 0;
+    if (++kt < (kPhased ? kend : st.nk)) return;
     ++t;
     new_step = true;
     seek(P, U);
@@ -782,7 +809,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         kvh_of = U.bhk;
         ok = mbar_wait(bar(kBarQEmpty), (uc & 1) ^ 1, abort_flag, err) && slot_free(0);
         if (!ok) break;
-        TileIter<kSegMode> it;
+        TileIter<kSegMode, kMaskable> it;
         it.begin(P, U);
         // Q tiles and K_0 on q_full
         mbar_arrive_expect_tx(bar(kBarQFull), 3 * kTileBytes);
@@ -984,13 +1011,15 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
       int pend = 0;         // reference move (log2 units) due before the next tile
       float l = 0.f;   // row sum of p as computed (log-sum-exp)
       float lr = 0.f;  // row sum of p rounded to bf16 (normalisation)
-      TileIter<kSegMode> it;
+      TileIter<kSegMode, kMaskable> it;
       it.begin(P, U);
       int64_t row_lim = 0;
-      for (int j = 0; j < n; ++j) {
+      // one key tile; kM: the masked softmax compiled in (phase 1 tiles)
+      auto tile = [&](int j, auto masked) -> bool {
+        constexpr bool kM = decltype(masked)::value;
         ok = __all_sync(0xffffffffu,
                         mbar_wait(bar(kBarSFull + i), (uint32_t)((gt + j) & 1), abort_flag, err));
-        if (!ok) break;
+        if (!ok) return false;
         tc_fence_after();
         if (releaser) {
           const uint64_t kp = kvpos + 2 * (uint64_t)j;  // K_j
@@ -999,10 +1028,13 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
           if (j == n - 1) mbar_arrive(bar(kBarQEmpty));
         }
         // last visible column of this tile for this row
-        if (it.new_step) row_lim = step_row_limit<kSegMode>(P, it.st, a_row);
-        const int64_t lim = row_lim - (int64_t)it.kt * kBN;
-        const int vis_max = (int)max((int64_t)-1, min(lim, (int64_t)(kBN - 1)));
-        const bool need_mask = kMaskable && __any_sync(0xffffffffu, vis_max < kBN - 1);
+        int vis_max = kBN - 1;
+        if constexpr (kM) {
+          if (it.new_step) row_lim = step_row_limit<kSegMode>(P, it.st, a_row);
+          const int64_t lim = row_lim - (int64_t)it.kt * kBN;
+          vis_max = (int)max((int64_t)-1, min(lim, (int64_t)(kBN - 1)));
+        }
+        const bool need_mask = kM && __any_sync(0xffffffffu, vis_max < kBN - 1);
         // O *= f for this row (online max: the reference moved up)
         auto rescale_o = [&](float f) {
 #pragma unroll 1
@@ -1088,7 +1120,15 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         tc_fence_before();
         mbar_arrive(bar(kBarPFull + i));
         it.next(P, U);
-      }
+        return true;
+      };
+      int j = 0;
+      if (kMaskable)
+        for (; j < n && it.phase == 0; ++j)
+          if (!tile(j, std::false_type{})) break;
+      if (ok)
+        for (; j < n; ++j)
+          if (!tile(j, std::integral_constant<bool, kMaskable>{})) break;
       if (!ok) break;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarOFull + i), uc & 1, abort_flag, err));
       if (!ok) break;
