@@ -588,7 +588,7 @@ __device__ __forceinline__ float2 tile_sums(const RowSums& rs) {
 // registers (pk) and summed into rs, while the row maximum of the raw scores
 // is tracked.  Nothing is written to TMEM, so if the maximum turns out to lie
 // more than 64 (log2) above the reference the caller still has S to start
-// over from.  (Masked tiles take the two-pass path, out of line.)
+// over from.  (Masked tiles have their own single pass, spec_row_masked.)
 __device__ __forceinline__ float spec_row(uint32_t tS, uint64_t sl2_2, uint64_t nref_2,
                                           uint32_t (&pk)[64], RowSums& rs) {
   uint32_t ra[32], rb[32];
@@ -700,11 +700,12 @@ __device__ __noinline__ void rescale_o_row(uint32_t tO, float f) {
 }
 
 // The masked row passes, out of line: masked tiles are a few per cent of a
-// causal problem's tiles, and keeping their code out of the loop keeps the
-// unmasked tile's code compact (same-process A/B: causal contiguous 22.03 ->
-// 21.29 ms, striped 22.56 -> 22.11 ms, DCP prefill 10.67 -> 10.39 ms).  In
-// online mode a masked tile takes the two-pass path (maximum, then exp), so
-// the speculative single pass exists only unmasked.
+// causal problem's tiles, and keeping their code out of line keeps the loop
+// over them compact (same-process A/B, when masked and unmasked tiles shared
+// one loop: causal contiguous 22.03 -> 21.29 ms, striped 22.56 -> 22.11 ms,
+// DCP prefill 10.67 -> 10.39 ms).  Const max runs every masked tile through
+// the exp pass; online max runs both passes on a unit's first tile and on the
+// rare tile whose maximum outruns the speculative pass.
 __device__ __noinline__ float row_max_masked(uint32_t tS, int vis_max) {
   return row_max_from_tmem<true>(tS, vis_max);
 }
@@ -714,6 +715,68 @@ __device__ __noinline__ float2 exp_row_masked(uint32_t tS, int vis_max, float sl
 // The same without the rounded row sum, for rows that see many keys in all.
 __device__ __noinline__ float2 exp_row_masked_plain(uint32_t tS, int vis_max, float sl2, float ref) {
   return exp_row_to_tmem<true, false>(tS, vis_max, sl2, ref);
+}
+
+// Online max, speculative single pass over one S row of a masked tile (the
+// masked counterpart of spec_row, inlined only into the loop over a unit's
+// masked tiles): each 32-column chunk is classified across the warp as in
+// exp_chunk_masked, p is formed against the current reference m and kept in
+// registers while the visible maximum is tracked.  If no row of the warp has
+// its maximum more than 64 (log2) above m, P is written to TMEM and (l, lr,
+// pending reference move as int bits, 1) is returned; otherwise nothing is
+// written and .w is 0, and the caller takes the two-pass path over the
+// intact S.  lr sums the bf16-rounded p when kInl.
+template <bool kInl>
+__device__ __forceinline__ float4 spec_row_masked(uint32_t tS, int vis_max, float sl2, float m) {
+  const uint64_t sl2_2 = f2_pack(sl2, sl2), nref_2 = f2_pack(-m, -m);
+  RowSums rs{f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+  uint32_t pk[64];
+  uint32_t ra[32], rb[32];
+  float mx = -INFINITY;
+  auto chunk = [&](const uint32_t(&r)[32], int ch) {
+    if (__all_sync(0xffffffffu, ch * 32 + 31 <= vis_max)) {
+      mx = chunk_max<false>(r, ch * 32, kBN - 1, mx);
+#pragma unroll
+      for (int x = 0; x < 16; ++x)
+        pk[16 * ch + x] = exp_pair<kInl>(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1]), sl2_2,
+                                         nref_2, rs);
+    } else if (__all_sync(0xffffffffu, ch * 32 > vis_max)) {
+#pragma unroll
+      for (int x = 0; x < 16; ++x) pk[16 * ch + x] = 0u;
+    } else {
+      mx = chunk_max<true>(r, ch * 32, vis_max, mx);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) {
+        float s0 = __uint_as_float(r[2 * x]), s1 = __uint_as_float(r[2 * x + 1]);
+        if (ch * 32 + 2 * x > vis_max) s0 = -INFINITY;
+        if (ch * 32 + 2 * x + 1 > vis_max) s1 = -INFINITY;
+        pk[16 * ch + x] = exp_pair<kInl>(s0, s1, sl2_2, nref_2, rs);
+      }
+    }
+  };
+  tmem_ld32(tS, ra);
+  tmem_ld_wait();
+  reg_fence(ra);
+  tmem_ld32(tS + 32, rb);
+  chunk(ra, 0);
+  tmem_ld_wait();
+  reg_fence(rb);
+  tmem_ld32(tS + 64, ra);
+  chunk(rb, 1);
+  tmem_ld_wait();
+  reg_fence(ra);
+  tmem_ld32(tS + 96, rb);
+  chunk(ra, 2);
+  tmem_ld_wait();
+  reg_fence(rb);
+  chunk(rb, 3);
+  const float jump = mx * sl2 - m;
+  if (!__all_sync(0xffffffffu, !(jump > 64.f))) return make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) tmem_st16(tS + ch * 16, &pk[16 * ch]);
+  const float2 t = tile_sums<kInl>(rs);
+  const int pend = jump > kRescaleThreshold ? (int)ceilf(jump) : 0;
+  return make_float4(t.x, t.y, __int_as_float(pend), 1.f);
 }
 
 // kConst: the const-max instantiation (no running maximum) or the online-max
@@ -1064,6 +1127,17 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         }
         if (const_max) {
           mref = c_log2;
+        } else if (need_mask && j > 0 && !__any_sync(0xffffffffu, m == -INFINITY)) {
+          // a masked tile after the first: the single pass, with the mask
+          const float4 r = few_keys ? spec_row_masked<true>(tS, vis_max, P.scale_log2, m)
+                                    : spec_row_masked<false>(tS, vis_max, P.scale_log2, m);
+          if (r.w != 0.f) {
+            tl = r.x;
+            tlr = r.y;
+            pend = __float_as_int(r.z);
+            p_done = true;
+          }
+          mref = m;
         } else if (!need_mask && j > 0 && !__any_sync(0xffffffffu, m == -INFINITY)) {
           // within a unit the row maximum rarely moves past the lazy-rescale
           // threshold: try the single pass against the current reference
