@@ -896,9 +896,11 @@ def run_profile_case(args):
     from context_attention_gb300 import synth
 
     torch.cuda.set_device(0)
-    if args.profile == "ring":
-        # DiT recipe with 16 heads: q,k,v 201 MB (> L2), one launch ~2 ms
-        q, k, v = synth.dit_qk(1, 16, PREFILL["S"], PREFILL["D"], seed=PREFILL["seed"], device="cuda")
+    if args.profile in ("ring", "ring_dit"):
+        # DiT recipe with 16 heads: q,k,v 201 MB (> L2), one launch ~1.2 ms;
+        # ring_dit: the bench workload itself (40 heads, q,k,v 503 MB), ~3.2 ms
+        heads = PREFILL["H"] if args.profile == "ring_dit" else 16
+        q, k, v = synth.dit_qk(1, heads, PREFILL["S"], PREFILL["D"], seed=PREFILL["seed"], device="cuda")
         km = ca.key_max2(k)
         for _ in range(args.warmup + 1):
             ca.ring_attn_fwd_kmax(q, k, v, km, PREFILL["cp"])
@@ -1021,7 +1023,7 @@ def run_ours(args):
         "pct_of_bf16_peak": round(100.0 * value / world / peak, 2),
         "roofline": {"kernel": "ring_tc_kernel", "bound": "tensor", "achieved": round(ring_tflops, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(ring_tflops / peak, 4),
-                     "traffic": read_traffic("ring_tc_kernel_dit16k.txt"),
+                     "traffic": read_traffic("ring_tc_kernel_dit40h.txt"),
                      "peak_source": f"{peak_src} {'sustained' if long_run else 'burst'} bf16 "
                                     f"(timed region {total_ms / 1e3:.2f} s)",
                      "frac_of_burst": round(ring_tflops / peaks["bf16_tflops"], 4),
@@ -1142,8 +1144,8 @@ def main():
                     help="oracle seconds of the headline workload's CPU baseline")
     ap.add_argument("--cpu-seconds-each", type=float, default=3.0,
                     help="oracle seconds of each other workload's CPU baseline (decode and other_workloads)")
-    ap.add_argument("--profile", choices=["ring", "causal_contiguous", "causal_striped", "decode", "decode_small",
-                                          "prologue", "key_pass", "merge", "paged", "ring_decode"],
+    ap.add_argument("--profile", choices=["ring", "ring_dit", "causal_contiguous", "causal_striped", "decode",
+                                          "decode_small", "prologue", "key_pass", "merge", "paged", "ring_decode"],
                     default=None,
                     help="run one small launch of one kernel (for ncu captures) and exit")
     args = ap.parse_args()
