@@ -1074,8 +1074,9 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
       int pend = 0;         // reference move (log2 units) due before the next tile
       float l = 0.f;   // row sum of p as computed (log-sum-exp)
       float lr = 0.f;  // row sum of p rounded to bf16 (normalisation)
+      // the key tile each softmax step is on: only the masked path needs it
       TileIter<kSegMode, kMaskable> it;
-      it.begin(P, U);
+      if (kMaskable) it.begin(P, U);
       int64_t row_lim = 0;
       // one key tile; kM: the masked softmax compiled in (phase 1 tiles)
       auto tile = [&](int j, auto masked) -> bool {
@@ -1193,7 +1194,7 @@ ring_tc_kernel(const __grid_constant__ TcMaps maps, const TcParams P) {
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(kBarPFull + i));
-        it.next(P, U);
+        if (kMaskable) it.next(P, U);
         return true;
       };
       int j = 0;
