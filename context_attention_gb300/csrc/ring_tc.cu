@@ -18,8 +18,11 @@
 //                    TMEM, applies mask, shift and exp2, keeps the row sum in
 //                    a register, writes P (bf16) back over S in TMEM, and at
 //                    the end normalises O and writes o and lse;
-//   warp 8           TMA producer: Q tiles, then K and V tiles of every ring
-//                    step in order, through a 5-slot ring of 32 KB buffers;
+//   warp 8           TMA producer: Q tiles, then K and V tiles of the unit's
+//                    ring steps, through a 5-slot ring of 32 KB buffers --
+//                    first, step by step, the tiles every row of the unit
+//                    sees whole, then the tiles a causal or ragged-end mask
+//                    crosses, which the softmax runs in a loop of their own;
 //   warp 9           tcgen05 issuer: the whole warp walks the schedule (its
 //                    descriptors stay warp-uniform) and lane 0 issues
 //                    S_i = Q_i K^T and O_i += P_i V for both tiles,
