@@ -77,3 +77,27 @@ def test_prefill_and_prologue_baselines():
     check(bench.oracle_dcp_prefill_baseline(q, kp, vp, kc, vc, 16, 1024, 0.1), "TFLOP/s")
     x_q, x_k, x_v, g_q, g_k, cos, sin = synth.qkv_activations(1, 256, 4, 4, 128, 27)
     check(bench.oracle_prologue_baseline(x_q, x_k, x_v, g_q, g_k, cos, sin, 4, 4, 8, 0.1), "GB/s")
+
+
+def test_roofline_traffic_comes_from_committed_profiles():
+    """The bench reports each roofline's DRAM traffic from an ncu summary
+    under profiles/: every file it names exists and carries a per-launch
+    figure, and the figure is within a few per cent of the kernel's
+    algorithmic bytes (the ring kernel's q, k, v read and o, lse written at
+    the DiT size; the decode's valid K+V), so a renamed or stale summary
+    fails here rather than turning the field null."""
+    import inspect
+    import re
+
+    src = inspect.getsource(bench)
+    names = re.findall(r'read_traffic\("([^"]+)"\)', src)
+    assert names, "bench.py reads no traffic figure"
+    algorithmic = {
+        "ring_tc_kernel_dit40h.txt": (3 * 40 * 16384 * 128 * 2) + (40 * 16384 * 128 * 2 + 40 * 16384 * 4),
+        "dcp_decode_kernel_131k.txt": 2 * 4 * 64 * 8 * 32768 * 128 * 2,
+    }
+    for name in names:
+        v = bench.read_traffic(name)
+        assert v is not None, f"profiles/{name} has no traffic_bytes_per_launch"
+        if name in algorithmic:
+            assert abs(v / algorithmic[name] - 1.0) < 0.05, (name, v, algorithmic[name])
